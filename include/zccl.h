@@ -1,0 +1,178 @@
+/*
+ * zccl.h -- C ABI of libzccl, a GB300 (sm_103a) library for the lossless BF16
+ * exponent codec of "ZipCCL: Efficient Lossless Data Compression of
+ * Communication Collectives for Accelerating LLM Training" (technical
+ * summary sections 2.A-2.D of the page of that title).
+ *
+ * What the codec does (ZipCCL 2.A, 2.B): each BF16 value is split into a
+ * sign-mantissa byte and its 8-bit exponent; an exponent that is one of the
+ * 7 entries of a LUT becomes a 3-bit code 001..111, any other exponent gets
+ * the zero-point code 000 and is stored whole, in element order, in a
+ * separate zero-point array.  The LUT is derived from the standard deviation
+ * sigma of the tensor, so compression needs no statistics pass.
+ *
+ * Stream format (little-endian; every region a multiple of 128 bytes,
+ * ZipCCL 2.C).  Elements are cut into chunks of 4096; the last chunk keeps
+ * roundup(count, 1024) slots.
+ *   [0,128)    header: u32 magic 0x4C43435A ("ZCCL"), u16 version 1,
+ *              u16 log2(chunk) = 12, u64 n, u64 n_esc, u8 lut[7], u8 0,
+ *              u64 zp_offset, zeros
+ *   blocks     per chunk of L slots: L sign-mantissa bytes (sign in bit 7,
+ *              mantissa in bits 0..6), then 3 code planes of L/8 bytes; plane
+ *              p holds bit p of each code, slot s is bit (s mod 32) of the
+ *              little-endian 32-bit word s/32; padding slots are all zero
+ *   zp_offset  = 128 + 11 * (total slots) / 8: n_esc raw exponent bytes,
+ *              zero-padded to a multiple of 128
+ * Total size = zp_offset + roundup(n_esc, 128) bytes: 11 bits per element
+ * slot plus 8 bits per escape plus header and padding (ZipCCL 2.B: 16 -> 11
+ * bits).  No per-chunk offset table is stored: the decoder recounts escapes
+ * from the code planes and rescans.
+ *
+ * Conventions for every call:
+ *   - all calls are stateless and thread-safe, never throw, and never
+ *     allocate: the caller owns every buffer, including the workspace;
+ *   - device pointers refer to memory of the current CUDA device; data
+ *     buffers (inputs, outputs, streams, workspace) must be 16-byte aligned,
+ *     else ZCCL_ERR_INVALID_ARG; d_out_bytes must be 8-byte aligned;
+ *   - all device work is queued asynchronously on `stream`; errors the host
+ *     can see are returned at once and then nothing is launched;
+ *   - data-dependent errors (corrupt stream, bad segment, timeout) are
+ *     written to the optional device word *d_status (first error wins, by
+ *     compare-and-swap from 0).  The library never clears it: set it to 0
+ *     before the call and read it after the stream has synchronised;
+ *   - n is limited to 2^40 elements per stream.
+ *
+ * Workspace: a device buffer of zccl_workspace_bytes() bytes that the
+ * kernels use to order their chunks (a ticket counter and one flag word per
+ * chunk for the single-pass scan of escape counts).  It must be zeroed once
+ * before its first use (zccl_workspace_init or any memset to 0); every call
+ * leaves it ready for the next one.  A workspace must not be used by two
+ * calls that may run at the same time (different streams): they would race.
+ */
+#ifndef ZCCL_H
+#define ZCCL_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZCCL_OK = 0,
+    ZCCL_ERR_INVALID_ARG = 1,      /* bad pointer, alignment, size or LUT   */
+    ZCCL_ERR_BUFFER_TOO_SMALL = 2, /* output or workspace below the bound   */
+    ZCCL_ERR_CORRUPT_STREAM = 3,   /* header / escape count inconsistent    */
+    ZCCL_ERR_CUDA = 4,             /* a CUDA runtime call failed            */
+    ZCCL_ERR_TIMEOUT = 5           /* a bounded device wait ran out (~1 s)  */
+} zccl_status_t;
+
+/* exp[r] is the biased BF16 exponent coded as r+1 (codes 001..111). The 7
+ * bytes must be pairwise distinct. */
+typedef struct {
+    uint8_t exp[7];
+} zccl_lut_t;
+
+/* One segment of a batched compression: `n` BF16 values at device address
+ * `in` compressed into its own stream at device address `out`, which has
+ * room for `out_capacity` bytes (at least zccl_max_compressed_bytes(n)). */
+typedef struct {
+    const uint16_t* in;
+    uint64_t n;
+    void* out;
+    uint64_t out_capacity;
+} zccl_segment_t;
+
+/* Operation selector for zccl_workspace_bytes. */
+typedef enum {
+    ZCCL_OP_COMPRESS = 0,
+    ZCCL_OP_DECOMPRESS = 1,
+    ZCCL_OP_COMPRESS_BATCHED = 2,
+    ZCCL_OP_DECOMPRESS_REDUCE = 3
+} zccl_op_t;
+
+#define ZCCL_MAX_SEGMENTS 4096u /* segments per zccl_compress_batched call   */
+#define ZCCL_MAX_SHARDS 1024u   /* shards per zccl_decompress_reduce call    */
+
+/* LUT from sigma (ZipCCL 2.A): the 7 biased exponents E in 1..254 with the
+ * largest Gaussian binade mass 2(Phi(2^(k+1)/sigma) - Phi(2^k/sigma)),
+ * k = E - 127, computed in double; most probable first (exp[0] -> code 001);
+ * equal masses order by smaller E.  Host only.  Returns INVALID_ARG unless
+ * sigma is finite and > 0 and lut is non-NULL. */
+zccl_status_t zccl_lut_from_sigma(double sigma, zccl_lut_t* lut);
+
+/* Stream size when every element escapes: an upper bound for any input of
+ * n elements (ZipCCL 2.B sizes, 2.C padding).  Host only. */
+uint64_t zccl_max_compressed_bytes(uint64_t n);
+
+/* Byte offset of the zero-point array in a stream of n elements; it depends
+ * on n only, so header + chunk blocks of a stream have a size known before
+ * compression.  Host only. */
+uint64_t zccl_zero_point_offset(uint64_t n);
+
+/* Workspace bytes for one call of `op`.  n: elements (compress, decompress,
+ * decompress_reduce) or an upper bound of the segments' total elements
+ * (batched); k: segment count (batched) or shard count (reduce), else
+ * ignored.  Host only. */
+zccl_status_t zccl_workspace_bytes(int op, uint64_t n, uint32_t k, uint64_t* bytes);
+
+/* Zero a workspace on `stream` (one cudaMemsetAsync). */
+zccl_status_t zccl_workspace_init(void* d_ws, uint64_t ws_bytes, cudaStream_t stream);
+
+/* Compress (ZipCCL 2.B, 2.C): n BF16 values at d_in -> one stream at d_out.
+ * out_capacity must be >= zccl_max_compressed_bytes(n) (else
+ * BUFFER_TOO_SMALL).  The stream's byte size is written to *d_out_bytes
+ * (device).  Bytes of d_out past that size are not written. */
+zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* lut,
+                            void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes,
+                            void* d_ws, uint64_t ws_bytes, uint32_t* d_status,
+                            cudaStream_t stream);
+
+/* Decompress (inverse of ZipCCL 2.B): the stream of in_bytes bytes at d_in
+ * -> n BF16 values at d_out.  The host checks in_bytes >=
+ * zccl_zero_point_offset(n) (header and blocks present); the device checks
+ * magic, version, chunk size, n, zp_offset, that the zero-point array fits
+ * in in_bytes and that the escapes recounted from the code planes equal the
+ * header's n_esc, and reports CORRUPT_STREAM in *d_status otherwise (the
+ * output is then unspecified).  The header's LUT is used as stored. */
+zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n,
+                              void* d_ws, uint64_t ws_bytes, uint32_t* d_status,
+                              cudaStream_t stream);
+
+/* Batched compress of ragged segments in one launch (ZipCCL 2.D: the
+ * static and dynamic parts of an MoE all-to-all payload).  d_segs is a
+ * DEVICE array of n_segs descriptors (routing sizes never visit the host);
+ * total_n must be >= the sum of their n (it sizes the grid and the
+ * workspace; an undercount is reported as INVALID_ARG in *d_status and
+ * nothing is written).  Every segment becomes an independent stream, exactly
+ * what zccl_compress writes for it; its size goes to d_out_bytes[s]
+ * (device array of n_segs).  A segment with a misaligned pointer, n >= 2^40
+ * or too small a capacity is skipped: d_out_bytes[s] = 0 and *d_status
+ * gets INVALID_ARG or BUFFER_TOO_SMALL.  n_segs <= ZCCL_MAX_SEGMENTS. */
+zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_segs,
+                                    uint64_t total_n, const zccl_lut_t* lut,
+                                    uint64_t* d_out_bytes, void* d_ws, uint64_t ws_bytes,
+                                    uint32_t* d_status, cudaStream_t stream);
+
+/* Local reduction of the zipped all-to-all path of reduce-scatter (ZipCCL
+ * 2.D): decode S streams of n elements each and write
+ *   d_out[i] = RNE_bf16( (((x_0[i] + x_1[i]) + x_2[i]) + ... ) + x_{S-1}[i] )
+ * with every add in fp32 round-to-nearest (no FMA, no flush to zero), in
+ * shard order, rounded to nearest-even BF16; any NaN result becomes 0x7FC0.
+ * d_streams and d_in_bytes are DEVICE arrays of S entries; each stream keeps
+ * its own LUT.  Every stream must hold exactly n elements, else
+ * CORRUPT_STREAM.  1 <= S <= ZCCL_MAX_SHARDS. */
+zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_t* d_in_bytes,
+                                     uint32_t S, uint16_t* d_out, uint64_t n, void* d_ws,
+                                     uint64_t ws_bytes, uint32_t* d_status,
+                                     cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* zccl_status_string(zccl_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZCCL_H */

@@ -1,1 +1,158 @@
-"""lossless_bf16_exponent_split_gb300 -- GB300 lossless BF16 exponent codec."""
+"""lossless_bf16_exponent_split_gb300 -- Python binding of libzccl, the GB300
+lossless BF16 exponent codec ("ZipCCL: Efficient Lossless Data Compression of
+Communication Collectives for Accelerating LLM Training", technical summary
+2.A-2.D).
+
+The functions named ``zccl_*`` mirror the C ABI in ``include/zccl.h`` one to
+one: they only marshal arguments (integers are device addresses, streams are
+``cudaStream_t`` handles as integers) and return the C status code.  Every step
+of the codec runs in the library's CUDA kernels; there is no Python or CPU
+fallback -- if ``libzccl.so`` is missing, every call raises.
+
+``Codec`` is a convenience layer over the same calls that allocates buffers
+with PyTorch (device memory and streams only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+OK, INVALID_ARG, BUFFER_TOO_SMALL, CORRUPT_STREAM, CUDA_ERROR, TIMEOUT = range(6)
+OP_COMPRESS, OP_DECOMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS_REDUCE = range(4)
+MAX_SEGMENTS = 4096
+MAX_SHARDS = 1024
+CHUNK = 4096
+
+LIB_PATH = _build.LIB
+_lib = None
+_lock = threading.Lock()
+
+# C function signatures: name -> (argtypes, restype)
+_u8p = ctypes.c_void_p
+_SIGS = {
+    "zccl_lut_from_sigma": ([ctypes.c_double, ctypes.c_void_p], ctypes.c_int),
+    "zccl_max_compressed_bytes": ([ctypes.c_uint64], ctypes.c_uint64),
+    "zccl_zero_point_offset": ([ctypes.c_uint64], ctypes.c_uint64),
+    "zccl_workspace_bytes": ([ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32,
+                              ctypes.POINTER(ctypes.c_uint64)], ctypes.c_int),
+    "zccl_workspace_init": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p], ctypes.c_int),
+    "zccl_compress": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
+                       ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "zccl_decompress": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
+                         ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p],
+                        ctypes.c_int),
+    "zccl_compress_batched": ([ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                               ctypes.c_void_p], ctypes.c_int),
+    "zccl_decompress_reduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
+                                ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                                ctypes.c_void_p], ctypes.c_int),
+    "zccl_status_string": ([ctypes.c_int], ctypes.c_char_p),
+}
+
+
+class ZcclError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libzccl (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libzccl not built ({LIB_PATH} missing): run "
+                                   "lossless_bf16_exponent_split_gb300.build.build()")
+            cdll = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(cdll, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = cdll
+        return _lib
+
+
+def _lut_buf(lut) -> ctypes.Array:
+    b = bytes(lut)
+    if len(b) != 7:
+        raise ValueError("a LUT is 7 exponent bytes")
+    return (ctypes.c_uint8 * 7)(*b)
+
+
+# ---- the C ABI, one to one ---------------------------------------------------
+def zccl_lut_from_sigma(sigma: float) -> bytes:
+    buf = (ctypes.c_uint8 * 7)()
+    st = lib().zccl_lut_from_sigma(float(sigma), ctypes.byref(buf))
+    if st != OK:
+        raise ZcclError(st, "zccl_lut_from_sigma")
+    return bytes(buf)
+
+
+def zccl_max_compressed_bytes(n: int) -> int:
+    return int(lib().zccl_max_compressed_bytes(n))
+
+
+def zccl_zero_point_offset(n: int) -> int:
+    return int(lib().zccl_zero_point_offset(n))
+
+
+def zccl_workspace_bytes(op: int, n: int, k: int = 0) -> int:
+    out = ctypes.c_uint64(0)
+    st = lib().zccl_workspace_bytes(op, n, k, ctypes.byref(out))
+    if st != OK:
+        raise ZcclError(st, "zccl_workspace_bytes")
+    return int(out.value)
+
+
+def zccl_workspace_init(d_ws: int, ws_bytes: int, stream: int) -> int:
+    return lib().zccl_workspace_init(d_ws, ws_bytes, stream)
+
+
+def zccl_compress(d_in, n, lut, d_out, out_capacity, d_out_bytes, d_ws, ws_bytes, d_status,
+                  stream) -> int:
+    return lib().zccl_compress(d_in, n, ctypes.byref(_lut_buf(lut)), d_out, out_capacity,
+                               d_out_bytes, d_ws, ws_bytes, d_status, stream)
+
+
+def zccl_decompress(d_in, in_bytes, d_out, n, d_ws, ws_bytes, d_status, stream) -> int:
+    return lib().zccl_decompress(d_in, in_bytes, d_out, n, d_ws, ws_bytes, d_status, stream)
+
+
+def zccl_compress_batched(d_segs, n_segs, total_n, lut, d_out_bytes, d_ws, ws_bytes, d_status,
+                          stream) -> int:
+    return lib().zccl_compress_batched(d_segs, n_segs, total_n, ctypes.byref(_lut_buf(lut)),
+                                       d_out_bytes, d_ws, ws_bytes, d_status, stream)
+
+
+def zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes, d_status,
+                           stream) -> int:
+    return lib().zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes,
+                                        d_status, stream)
+
+
+def zccl_status_string(status: int) -> str:
+    return lib().zccl_status_string(status).decode()
+
+
+def status_string(status: int) -> str:
+    try:
+        return zccl_status_string(status)
+    except Exception:  # library missing: still give a readable message
+        return "unknown"
+
+
+def check(status: int, what: str) -> None:
+    if status != OK:
+        raise ZcclError(status, what)
+
+
+from .codec import Codec  # noqa: E402  (torch-based convenience layer)
+
+__all__ = [n for n in list(globals()) if n.startswith("zccl_")] + [
+    "Codec", "ZcclError", "check", "lib", "status_string"]

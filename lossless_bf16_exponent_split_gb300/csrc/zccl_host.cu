@@ -1,0 +1,252 @@
+// zccl_host.cu -- the C ABI of libzccl: argument validation, LUT derivation,
+// workspace sizing and kernel launches.  Declarations and contracts are in
+// include/zccl.h.
+//
+// Page: "ZipCCL: Efficient Lossless Data Compression of Communication
+// Collectives for Accelerating LLM Training", technical summary 2.A (LUT
+// from the layer's sigma instead of an online histogram) and 2.B-2.D (the
+// operations this layer launches).
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "zccl_common.cuh"
+#include "zccl_internal.h"
+
+using namespace zccl;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    int sms = 0;
+    int compress_per_sm = 1;
+    int compress_per_sm_batched = 1;
+    int decompress_per_sm = 1;
+    int reduce_per_sm_small = 1;  // S <= kSmallShards
+    int reduce_per_sm_large = 1;  // any S <= ZCCL_MAX_SHARDS
+};
+constexpr uint32_t kSmallShards = 32;
+DeviceInfo g_dev[kMaxDevices];
+
+// SM count and kernel occupancy of the current device, computed once.
+const DeviceInfo* device_info()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceInfo& d = g_dev[dev];
+    std::call_once(d.once, [&]() {
+        int sms = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        d.sms = sms > 0 ? sms : 1;
+        d.compress_per_sm = compress_ctas_per_sm(1);
+        d.compress_per_sm_batched = compress_ctas_per_sm(ZCCL_MAX_SEGMENTS);
+        d.decompress_per_sm = decompress_ctas_per_sm();
+        d.reduce_per_sm_small = reduce_ctas_per_sm(kSmallShards);
+        d.reduce_per_sm_large = reduce_ctas_per_sm(ZCCL_MAX_SHARDS);
+    });
+    return &d;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+bool lut_ok(const zccl_lut_t* lut)
+{
+    if (lut == nullptr) return false;
+    for (int i = 0; i < 7; ++i)
+        for (int j = i + 1; j < 7; ++j)
+            if (lut->exp[i] == lut->exp[j]) return false;
+    return true;
+}
+
+uint64_t ws_bytes_for_units(uint64_t units) { return round_up(kCtrlBytes + 8 * units, 256); }
+
+uint32_t grid_for(uint64_t units, int per_sm, int sms)
+{
+    const uint64_t cap = (uint64_t)per_sm * (uint64_t)sms;
+    const uint64_t g = std::min<uint64_t>(units, cap);
+    return (uint32_t)std::max<uint64_t>(g, 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+zccl_status_t zccl_lut_from_sigma(double sigma, zccl_lut_t* lut)
+{
+    if (lut == nullptr || !(sigma > 0.0) || !std::isfinite(sigma)) return ZCCL_ERR_INVALID_ARG;
+    // Gaussian mass of every normal binade E = 1..254, then the 7 largest.
+    struct Cand {
+        double mass;
+        int e;
+    };
+    Cand c[254];
+    const double inv = 1.0 / (sigma * std::sqrt(2.0));
+    for (int e = 1; e <= 254; ++e) {
+        const double a = std::ldexp(1.0, e - 127), b = std::ldexp(1.0, e - 126);
+        // 2 (Phi(b/sigma) - Phi(a/sigma)) = erfc(a/(sigma sqrt 2)) - erfc(b/(sigma sqrt 2))
+        c[e - 1] = Cand{std::erfc(a * inv) - std::erfc(b * inv), e};
+    }
+    std::partial_sort(c, c + 7, c + 254, [](const Cand& x, const Cand& y) {
+        return x.mass != y.mass ? x.mass > y.mass : x.e < y.e;
+    });
+    for (int r = 0; r < 7; ++r) lut->exp[r] = (uint8_t)c[r].e;
+    return ZCCL_OK;
+}
+
+uint64_t zccl_max_compressed_bytes(uint64_t n) { return stream_bytes_of(n, n); }
+
+uint64_t zccl_zero_point_offset(uint64_t n) { return zp_offset_of(n); }
+
+zccl_status_t zccl_workspace_bytes(int op, uint64_t n, uint32_t k, uint64_t* bytes)
+{
+    if (bytes == nullptr || n >= kMaxElems) return ZCCL_ERR_INVALID_ARG;
+    switch (op) {
+        case ZCCL_OP_COMPRESS:
+        case ZCCL_OP_DECOMPRESS: *bytes = ws_bytes_for_units(units_of(n)); return ZCCL_OK;
+        case ZCCL_OP_COMPRESS_BATCHED:
+            if (k == 0 || k > ZCCL_MAX_SEGMENTS) return ZCCL_ERR_INVALID_ARG;
+            *bytes = ws_bytes_for_units(n / kChunk + k);
+            return ZCCL_OK;
+        case ZCCL_OP_DECOMPRESS_REDUCE:
+            if (k == 0 || k > ZCCL_MAX_SHARDS) return ZCCL_ERR_INVALID_ARG;
+            *bytes = ws_bytes_for_units(units_of(n) * k);
+            return ZCCL_OK;
+        default: return ZCCL_ERR_INVALID_ARG;
+    }
+}
+
+zccl_status_t zccl_workspace_init(void* d_ws, uint64_t ws_bytes, cudaStream_t stream)
+{
+    if (d_ws == nullptr || ws_bytes < kCtrlBytes) return ZCCL_ERR_INVALID_ARG;
+    return cudaMemsetAsync(d_ws, 0, ws_bytes, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* lut, void* d_out,
+                            uint64_t out_capacity, uint64_t* d_out_bytes, void* d_ws, uint64_t ws_bytes,
+                            uint32_t* d_status, cudaStream_t stream)
+{
+    if (n >= kMaxElems || !lut_ok(lut) || d_out == nullptr || !aligned(d_out, 16) ||
+        (n > 0 && (d_in == nullptr || !aligned(d_in, 16))) || d_out_bytes == nullptr ||
+        !aligned(d_out_bytes, 8) || d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+        return ZCCL_ERR_INVALID_ARG;
+    if (out_capacity < zccl_max_compressed_bytes(n)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const uint64_t units = units_of(n);
+    if (ws_bytes < ws_bytes_for_units(units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+
+    CompressArgs a{};
+    a.segs = nullptr;
+    a.single = zccl_segment_t{d_in, n, d_out, out_capacity};
+    a.n_segs = 1;
+    a.max_units = (uint32_t)units;
+    std::memcpy(a.lut, lut->exp, 7);
+    a.out_bytes = d_out_bytes;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.status = d_status;
+    const uint32_t grid = grid_for(units, dev->compress_per_sm, dev->sms);
+    return launch_compress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_segs, uint64_t total_n,
+                                    const zccl_lut_t* lut, uint64_t* d_out_bytes, void* d_ws,
+                                    uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream)
+{
+    if (n_segs == 0 || n_segs > ZCCL_MAX_SEGMENTS || total_n >= kMaxElems || !lut_ok(lut) ||
+        d_segs == nullptr || !aligned(d_segs, 8) || d_out_bytes == nullptr || !aligned(d_out_bytes, 8) ||
+        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+        return ZCCL_ERR_INVALID_ARG;
+    const uint64_t max_units = total_n / kChunk + n_segs;
+    if (ws_bytes < ws_bytes_for_units(max_units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+
+    CompressArgs a{};
+    a.segs = d_segs;
+    a.n_segs = n_segs;
+    a.max_units = (uint32_t)max_units;
+    std::memcpy(a.lut, lut->exp, 7);
+    a.out_bytes = d_out_bytes;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.status = d_status;
+    const uint32_t grid = grid_for(max_units, dev->compress_per_sm_batched, dev->sms);
+    return launch_compress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n, void* d_ws,
+                              uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream)
+{
+    if (n >= kMaxElems || d_in == nullptr || !aligned(d_in, 16) || (n > 0 && (d_out == nullptr || !aligned(d_out, 16))) ||
+        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+        return ZCCL_ERR_INVALID_ARG;
+    if (in_bytes < zp_offset_of(n)) return ZCCL_ERR_INVALID_ARG;
+    const uint64_t units = units_of(n);
+    if (ws_bytes < ws_bytes_for_units(units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+
+    DecompressArgs a{};
+    a.in = reinterpret_cast<const uint8_t*>(d_in);
+    a.in_bytes = in_bytes;
+    a.out = d_out;
+    a.n = n;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.status = d_status;
+    const uint32_t grid = grid_for(units, dev->decompress_per_sm, dev->sms);
+    return launch_decompress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
+                                     uint16_t* d_out, uint64_t n, void* d_ws, uint64_t ws_bytes,
+                                     uint32_t* d_status, cudaStream_t stream)
+{
+    if (S == 0 || S > ZCCL_MAX_SHARDS || n >= kMaxElems || d_streams == nullptr || !aligned(d_streams, 8) ||
+        d_in_bytes == nullptr || !aligned(d_in_bytes, 8) || (n > 0 && (d_out == nullptr || !aligned(d_out, 16))) ||
+        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+        return ZCCL_ERR_INVALID_ARG;
+    const uint64_t units = units_of(n);
+    if (ws_bytes < ws_bytes_for_units(units * S)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+
+    ReduceArgs a{};
+    a.streams = d_streams;
+    a.in_bytes = d_in_bytes;
+    a.S = S;
+    a.out = d_out;
+    a.n = n;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.status = d_status;
+    const int per_sm = S <= kSmallShards ? dev->reduce_per_sm_small : dev->reduce_per_sm_large;
+    const uint32_t grid = grid_for(units, per_sm, dev->sms);
+    return launch_reduce(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+}
+
+const char* zccl_status_string(zccl_status_t s)
+{
+    switch (s) {
+        case ZCCL_OK: return "ok";
+        case ZCCL_ERR_INVALID_ARG: return "invalid argument";
+        case ZCCL_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+        case ZCCL_ERR_CORRUPT_STREAM: return "corrupt stream";
+        case ZCCL_ERR_CUDA: return "CUDA runtime error";
+        case ZCCL_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

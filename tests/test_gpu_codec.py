@@ -1,0 +1,172 @@
+"""GPU parity: libzccl compress/decompress against the oracle, byte for byte.
+
+The oracle (plain C, CPU) defines the stream; the CUDA kernels must produce
+identical stream bytes and identical decoded bits (ZipCCL technical summary
+2.B, 2.C: lossless, bit-exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from golden_io import read_stream_fixture
+from gpu_util import dev_bytes, dev_u16, host_u16, load_lib, require_gpu, stream_of
+from lossless_bf16_exponent_split_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+LUTS = {
+    "sigma0.02": oracle.lut_from_sigma(0.02),
+    "sigma1": oracle.lut_from_sigma(1.0),
+    "zero_inf": bytes([0, 255, 1, 2, 3, 254, 127]),
+    "absent": bytes([200, 201, 202, 203, 204, 205, 206]),
+}
+EDGE_N = [0, 1, 7, 8, 9, 31, 32, 33, 1023, 1024, 1025, 4095, 4096, 4097, 8191, 8192,
+          3 * 4096 + 5, 10 * 4096 + 1000, 100_003]
+
+
+@pytest.fixture(scope="module")
+def codec():
+    require_gpu()
+    load_lib()
+    from lossless_bf16_exponent_split_gb300 import Codec
+    return Codec()
+
+
+def gpu_compress(codec, x, lut):
+    codec.reset_status()
+    out, nb = codec.compress(dev_u16(x), lut)
+    s = stream_of(out, nb)
+    assert codec.read_status() == 0
+    return s
+
+
+def gpu_decompress(codec, stream, n):
+    codec.reset_status()
+    y = codec.decompress(dev_bytes(stream), len(stream), n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    return host_u16(y)
+
+
+@pytest.mark.parametrize("n", EDGE_N)
+@pytest.mark.parametrize("lut_name", ["sigma0.02", "zero_inf"])
+def test_compress_edge_sizes(codec, n, lut_name):
+    x = workloads.special_values(n, seed=n) if lut_name == "zero_inf" else workloads.gaussian(n, 0.02, seed=n)
+    lut = LUTS[lut_name]
+    want = oracle.compress(x, lut)
+    assert gpu_compress(codec, x, lut) == want
+    assert np.array_equal(gpu_decompress(codec, want, n), x)
+
+
+@pytest.mark.parametrize("lut_name", list(LUTS))
+def test_all_bf16_patterns(codec, lut_name):
+    x = np.arange(65536, dtype=np.uint16)
+    lut = LUTS[lut_name]
+    want = oracle.compress(x, lut)
+    assert gpu_compress(codec, x, lut) == want
+    assert np.array_equal(gpu_decompress(codec, want, x.size), x)
+    # shuffled, so every chunk mixes every exponent
+    rng = np.random.default_rng(1)
+    xs = x[rng.permutation(x.size)]
+    want = oracle.compress(xs, lut)
+    assert gpu_compress(codec, xs, lut) == want
+    assert np.array_equal(gpu_decompress(codec, want, xs.size), xs)
+
+
+def test_hand_built_fixture(codec):
+    x, lut, stream = read_stream_fixture()
+    assert gpu_compress(codec, x, lut) == stream
+    assert np.array_equal(gpu_decompress(codec, stream, x.size), x)
+
+
+def test_escape_extremes(codec):
+    x = workloads.random_bits(50_000, seed=4)
+    for lut in (LUTS["absent"], bytes([1, 2, 3, 4, 5, 6, 7])):
+        want = oracle.compress(x, lut)
+        assert gpu_compress(codec, x, lut) == want
+    lut = LUTS["sigma1"]
+    e = np.frombuffer(lut, np.uint8).astype(np.uint16)
+    y = (e[np.arange(50_000) % 7] << 7) | (np.arange(50_000, dtype=np.uint16) & 0x807F)
+    want = oracle.compress(y, lut)
+    assert int.from_bytes(want[16:24], "little") == 0
+    assert gpu_compress(codec, y, lut) == want
+    assert np.array_equal(gpu_decompress(codec, want, y.size), y)
+
+
+def test_gauss1m(codec):
+    cfg = workloads.CONFIGS["gauss1m"]
+    x = workloads.gaussian(cfg["n"], cfg["sigma"], seed=0)
+    lut = oracle.lut_from_sigma(cfg["sigma"])
+    want = oracle.compress(x, lut)
+    assert gpu_compress(codec, x, lut) == want
+    assert np.array_equal(gpu_decompress(codec, want, x.size), x)
+
+
+def _full_size(codec, x, lut):
+    """Byte-identical stream and bit-identical decode at a full config size;
+    compared on the device to keep host traffic small."""
+    want = oracle.compress(x, lut)
+    codec.reset_status()
+    xd = dev_u16(x)
+    out, nb = codec.compress(xd, lut)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    assert int(nb.item()) == len(want)
+    wd = dev_bytes(want)
+    assert torch.equal(out[: len(want)], wd)
+    codec.reset_status()
+    y = codec.decompress(wd, len(want), x.size)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    assert torch.equal(y, xd)
+
+
+def test_llama3_8b_allgather_full(codec):
+    cfg = workloads.CONFIGS["llama3_8b_allgather"]
+    _full_size(codec, workloads.gaussian(cfg["n"], cfg["sigma"], seed=0),
+               oracle.lut_from_sigma(cfg["sigma"]))
+
+
+def test_activation_mix_full(codec):
+    _full_size(codec, workloads.activation_mix(), oracle.lut_from_sigma(1.0))
+
+
+def test_output_canary_untouched(codec):
+    x = workloads.gaussian(20_000, 0.02, seed=9)
+    lut = LUTS["sigma0.02"]
+    want = oracle.compress(x, lut)
+    cap = oracle.max_bytes(x.size)
+    out = torch.full((cap + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    codec.reset_status()
+    _, nb = codec.compress(dev_u16(x), lut, out=out)
+    torch.cuda.synchronize()
+    assert int(nb.item()) == len(want)
+    host = out.cpu().numpy()
+    assert host[: len(want)].tobytes() == want
+    assert (host[len(want):] == 0xA5).all()
+
+
+def test_repeated_calls_same_workspace(codec):
+    lut = LUTS["sigma1"]
+    for i in range(40):
+        n = 1 + (i * 7919) % 60000
+        x = workloads.gaussian(n, 1.0, seed=100 + i)
+        want = oracle.compress(x, lut)
+        assert gpu_compress(codec, x, lut) == want
+        assert np.array_equal(gpu_decompress(codec, want, n), x)
+
+
+def test_in_place_graph_of_calls_no_sync(codec):
+    """Several calls queued back to back on one stream, one sync at the end."""
+    lut = LUTS["sigma0.02"]
+    xs = [workloads.gaussian(n, 0.02, seed=n) for n in (5000, 123_457, 4096 * 7, 77)]
+    outs = []
+    codec.reset_status()
+    for x in xs:
+        xd = dev_u16(x)
+        outs.append((x, *codec.compress(xd, lut)))
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    for x, out, nb in outs:
+        assert stream_of(out, nb) == oracle.compress(x, lut)

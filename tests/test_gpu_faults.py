@@ -1,0 +1,120 @@
+"""GPU error paths: host-side argument errors (nothing launched), corrupt
+streams reported through the device status word, and the bounded device
+wait running out (a chunk flag that nothing ever sets)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import dev_bytes, dev_u16, load_lib, require_gpu
+from lossless_bf16_exponent_split_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def z():
+    require_gpu()
+    load_lib()
+    import lossless_bf16_exponent_split_gb300 as z
+    return z
+
+
+def test_host_argument_errors(z):
+    lut = oracle.lut_from_sigma(1.0)
+    n = 4096
+    x = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    cap = z.zccl_max_compressed_bytes(n)
+    out = torch.zeros(cap + 16, dtype=torch.uint8, device="cuda")
+    nb = torch.zeros(1, dtype=torch.int64, device="cuda")
+    wsb = z.zccl_workspace_bytes(z.OP_COMPRESS, n)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = lambda **kw: dict(dict(d_in=x.data_ptr(), n=n, lut=lut, d_out=out.data_ptr(),
+                                  out_capacity=cap, d_out_bytes=nb.data_ptr(), d_ws=ws.data_ptr(),
+                                  ws_bytes=wsb, d_status=st.data_ptr(), stream=s), **kw)
+    assert z.zccl_compress(**args()) == z.OK
+    assert z.zccl_compress(**args(d_in=x.data_ptr() + 2)) == z.INVALID_ARG
+    assert z.zccl_compress(**args(d_out=out.data_ptr() + 8)) == z.INVALID_ARG
+    assert z.zccl_compress(**args(out_capacity=cap - 1)) == z.BUFFER_TOO_SMALL
+    assert z.zccl_compress(**args(ws_bytes=128)) == z.BUFFER_TOO_SMALL
+    assert z.zccl_compress(**args(lut=bytes([1, 1, 2, 3, 4, 5, 6]))) == z.INVALID_ARG
+    assert z.zccl_compress(**args(n=1 << 40)) == z.INVALID_ARG
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+
+
+def _decode_status(z, stream: bytes, n: int, in_bytes=None):
+    codec = z.Codec()
+    codec.reset_status()
+    codec.decompress(dev_bytes(stream, pad=256), len(stream) if in_bytes is None else in_bytes, n)
+    torch.cuda.synchronize()
+    return codec.read_status()
+
+
+def _corrupt(stream, off, val):
+    b = bytearray(stream)
+    b[off] = val
+    return bytes(b)
+
+
+def _unescape_one(stream):
+    """Sets plane-0 bit of the first escaped slot of chunk 0, so the planes
+    hold one escape fewer than the header says."""
+    b = bytearray(stream)
+    planes = [np.unpackbits(np.frombuffer(bytes(b[128 + 4096 + p * 512: 128 + 4096 + (p + 1) * 512]),
+                                          np.uint8), bitorder="little") for p in range(3)]
+    slot = int(np.flatnonzero((planes[0] | planes[1] | planes[2]) == 0)[0])
+    b[128 + 4096 + slot // 8] |= 1 << (slot % 8)
+    return bytes(b)
+
+
+def test_corrupt_streams_reported(z):
+    x = workloads.gaussian(3 * 4096 + 500, 1.0, seed=1)
+    s = oracle.compress(x, oracle.lut_from_sigma(1.0))
+    n = x.size
+    assert _decode_status(z, s, n) == z.OK
+    for name, b in {
+        "magic": _corrupt(s, 0, 0),
+        "version": _corrupt(s, 4, 2),
+        "log2chunk": _corrupt(s, 6, 11),
+        "n": _corrupt(s, 8, s[8] ^ 1),
+        "n_esc_up": _corrupt(s, 16, s[16] + 1),
+        "n_esc_down": _corrupt(s, 16, s[16] - 1),
+        "zp_offset": _corrupt(s, 32, s[32] ^ 0x80),
+        "escape_made_coded": _unescape_one(s),
+    }.items():
+        assert oracle.decompress_status(b, n)[0] == oracle.CORRUPT, name
+        assert _decode_status(z, b, n) == z.CORRUPT_STREAM, name
+    # zero-point array cut off (in_bytes below the header's size)
+    assert _decode_status(z, s, n, in_bytes=len(s) - 128) == z.CORRUPT_STREAM
+
+
+def test_bounded_wait_times_out_and_workspace_recovers(z):
+    """Pre-set the workspace's ticket counter to 1: chunk 0 is never taken,
+    so its flag is never published and chunk 1's look-back waits on it.  The
+    wait is bounded (~1 s): the call must end with ZCCL_ERR_TIMEOUT, and the
+    workspace must be usable again by the next call."""
+    lut = oracle.lut_from_sigma(1.0)
+    n = 40 * 4096
+    x = workloads.gaussian(n, 1.0, seed=3)
+    codec = z.Codec()
+    codec.compress(dev_u16(x[:4096]), lut)  # creates the workspace
+    torch.cuda.synchronize()
+    wsb = z.zccl_workspace_bytes(z.OP_COMPRESS, n)
+    ws_ptr, _ = codec.workspace(wsb)
+    ctrl = codec._ws[:4].view(torch.int32)
+    ctrl.fill_(1)
+    codec.reset_status()
+    codec.compress(dev_u16(x), lut)
+    torch.cuda.synchronize()
+    assert codec.read_status() == z.TIMEOUT
+    assert int(codec._ws[:4].view(torch.int32).item()) == 0  # ticket reset by the last CTA
+    codec.reset_status()
+    out, nb = codec.compress(dev_u16(x), lut)
+    torch.cuda.synchronize()
+    assert codec.read_status() == z.OK
+    assert out[: int(nb.item())].cpu().numpy().tobytes() == oracle.compress(x, lut)
