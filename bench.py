@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the lossless BF16 exponent codec on GB300.
+
+Default workload: the Llama3-8B-shaped all-gather payload (one 4096x14336 BF16
+tensor, i.i.d. N(0, 0.02^2), LUT from sigma = 0.02).  One step = one pass of
+the codec's hot path over one batch: compress a batch, and decompress the
+stream compressed one step earlier (so the stream read by decompress is not
+L2-resident, as it would not be after crossing the network).  Three rotating
+buffer sets, 316 MB touched per step (> 129 MB L2), keep every step's inputs
+out of L2.  Other workloads (--workload): activation_mix (compress +
+decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
+rs_local (decompress-reduce of 8 shards), gauss1m.
+
+Prints ONE JSON line (rank 0).  `value` = GB/s of BF16 input through the step
+(2n bytes per compress and per decompress; reduce: 2 S n), whole job.
+`--impl reference` times the CPU oracle (plain C, single thread) instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="zccl", choices=["zccl", "reference"])
+    p.add_argument("--workload", default="llama3_8b_allgather",
+                   choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "gauss1m"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "lossless_bf16_exponent_split_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    with open(os.path.join(ROOT, "lossless_bf16_exponent_split_gb300", "csrc", "zccl_common.cuh"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"compress_kernel": ["zccl_compress.cu"], "decompress_kernel": ["zccl_decompress.cu"],
+                  "reduce_kernel": ["zccl_reduce.cu"]}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "zccl" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(pg, value: float, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg, device=None):
+    if pg is not None:
+        if device is not None:
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+# ---------------------------------------------------------------------------
+def workload_desc(name):
+    from lossless_bf16_exponent_split_gb300 import workloads
+    return workloads.CONFIGS[name]["desc"]
+
+
+def make_inputs(name, seed):
+    """Host arrays for a workload: (kind, payload(s), sigma, extra)."""
+    from lossless_bf16_exponent_split_gb300 import workloads as w
+    cfg = w.CONFIGS[name]
+    if name in ("llama3_8b_allgather", "gauss1m"):
+        return "roundtrip", w.gaussian(cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"], None
+    if name == "activation_mix":
+        return "roundtrip", w.activation_mix(seed=seed), cfg["sigma"], None
+    if name == "moe_a2a":
+        m = w.moe_payload(tokens=cfg["tokens"], top_k=cfg["top_k"], experts=cfg["experts"],
+                          hidden=cfg["hidden"], seed=seed)
+        return "batched", m.payload, cfg["sigma"], m
+    if name == "rs_local":
+        return "reduce", w.reduce_shards(cfg["S"], cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"], None
+    raise ValueError(name)
+
+
+def cpu_baseline(name, budget_s=12.0):
+    """The oracle as it stands (single-threaded C), on a bounded sample."""
+    import oracle
+    from lossless_bf16_exponent_split_gb300 import workloads as w
+    cfg = w.CONFIGS[name]
+    sigma = cfg["sigma"]
+    lut = oracle.lut_from_sigma(sigma)
+    if name == "rs_local":
+        n = 1 << 21
+        shards = w.reduce_shards(cfg["S"], n, sigma, seed=0)
+        streams = [oracle.compress(x, lut) for x in shards]
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.decompress_reduce(streams, n)
+            reps += 1
+            if time.perf_counter() - t0 > budget_s / 2:
+                break
+        dt = (time.perf_counter() - t0) / reps
+        return {"value": round(2 * cfg["S"] * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"decompress_reduce of {cfg['S']} shards x {n} elements, {reps} reps"}
+    n = 1 << 23
+    x = w.gaussian(n, sigma, seed=0) if name != "activation_mix" else w.activation_mix(2048, 4096)
+    n = x.size
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        s = oracle.compress(x, lut)
+        oracle.decompress(s, n)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s / 2:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    op = "compress (as batched segments) + decompress" if name == "moe_a2a" else "compress + decompress"
+    return {"value": round(2 * 2 * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{op} of the first {n} elements of the workload's distribution, {reps} reps"}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg_name = args.workload
+    from lossless_bf16_exponent_split_gb300 import workloads as w
+    cfg = w.CONFIGS[cfg_name]
+    lut = oracle.lut_from_sigma(cfg["sigma"])
+    # each step: a bounded sample of the workload (oracle speed ~0.1-0.3 GB/s)
+    if cfg_name == "rs_local":
+        n = 1 << 20
+        shards = w.reduce_shards(cfg["S"], n, cfg["sigma"], seed=0)
+        streams = [oracle.compress(x, lut) for x in shards]
+        step = lambda: oracle.decompress_reduce(streams, n)
+        unit_bytes = 2 * cfg["S"] * n
+        sample = f"decompress_reduce of {cfg['S']} shards x {n} elements per step"
+    else:
+        n = 1 << 21
+        x = w.gaussian(n, cfg["sigma"], seed=0)
+
+        def step():
+            s = oracle.compress(x, lut)
+            oracle.decompress(s, n)
+        unit_bytes = 2 * 2 * n
+        sample = f"compress + decompress of {n} elements of the workload's distribution per step"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = unit_bytes / dt / 1e9
+    line = {"metric": "compress/decompress GB/s of BF16 input", "value": round(v, 4), "unit": "GB/s",
+            "impl": "reference", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": cfg_name, "desc": cfg["desc"]},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import lossless_bf16_exponent_split_gb300 as z
+    from lossless_bf16_exponent_split_gb300 import build
+    build.build()
+    z.lib()
+
+    kind, host, sigma, extra = make_inputs(args.workload, seed=rank)
+    lut = z.zccl_lut_from_sigma(sigma)
+    stream = torch.cuda.current_stream()
+    h = int(stream.cuda_stream)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st_ptr = status.data_ptr()
+
+    def tdev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    launches_per_step = 0
+    kern = {}
+    if kind == "roundtrip":
+        n = host.size
+        R = 3
+        xs = [tdev(host) for _ in range(R)]
+        cap = z.zccl_max_compressed_bytes(n)
+        outs = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(R)]
+        nbs = [torch.zeros(1, dtype=torch.int64, device=dev) for _ in range(R)]
+        y = torch.empty(n, dtype=torch.int16, device=dev)
+        wsb = z.zccl_workspace_bytes(z.OP_COMPRESS, n)
+        ws_c = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+        ws_d = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+
+        def comp(r):
+            z.check(z.zccl_compress(xs[r].data_ptr(), n, lut, outs[r].data_ptr(), cap, nbs[r].data_ptr(),
+                                    ws_c.data_ptr(), wsb, st_ptr, h), "compress")
+
+        def decomp(r):
+            z.check(z.zccl_decompress(outs[r].data_ptr(), cap, y.data_ptr(), n, ws_d.data_ptr(), wsb, st_ptr, h),
+                    "decompress")
+
+        for r in range(R):
+            comp(r)
+        torch.cuda.synchronize()
+        stream_bytes = int(nbs[0].item())
+        launches_per_step = 2
+        names = ["compress_kernel", "decompress_kernel"]
+        alg = {"compress_kernel": 2 * n + stream_bytes, "decompress_kernel": stream_bytes + 2 * n}
+        step_input_bytes = 2 * 2 * n
+
+        def step(k, ev=None):
+            r = k % R
+            if ev:
+                ev[0].record(stream)
+            comp(r)
+            if ev:
+                ev[1].record(stream)
+            decomp((k - 1) % R)
+            if ev:
+                ev[2].record(stream)
+        cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
+                     "step": "compress batch k + decompress stream of batch k-1",
+                     "l2": "3 rotating buffer sets, >316 MB touched per step (> 129 MB L2)"}
+    elif kind == "batched":
+        m = extra
+        payload = tdev(host)
+        segs = []
+        hid = m.hidden
+        outs = []
+        for (r0, rows) in m.segments:
+            nn = rows * hid
+            cap = z.zccl_max_compressed_bytes(nn)
+            o = torch.empty(cap, dtype=torch.uint8, device=dev)
+            outs.append(o)
+            segs.append((payload[r0 * hid:(r0 + rows) * hid], o))
+        codec = z.Codec(dev)
+        table = codec.segment_table(segs)
+        total_n = host.size
+        nb = torch.zeros(len(segs), dtype=torch.int64, device=dev)
+        wsb = z.zccl_workspace_bytes(z.OP_COMPRESS_BATCHED, total_n, len(segs))
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+
+        def comp():
+            z.check(z.zccl_compress_batched(table.data_ptr(), len(segs), total_n, lut, nb.data_ptr(),
+                                            ws.data_ptr(), wsb, st_ptr, h), "compress_batched")
+        comp()
+        torch.cuda.synchronize()
+        sb = int(nb.sum().item())
+        launches_per_step = 1
+        names = ["compress_kernel"]
+        alg = {"compress_kernel": 2 * total_n + sb}
+        step_input_bytes = 2 * total_n
+
+        def step(k, ev=None):
+            if ev:
+                ev[0].record(stream)
+            comp()
+            if ev:
+                ev[1].record(stream)
+                ev[2].record(stream)
+        cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
+                     "step": "one batched compress of all static+dynamic segments",
+                     "l2": "input 537 MB > 129 MB L2"}
+    else:  # reduce
+        shards = host
+        S = len(shards)
+        n = shards[0].size
+        codec = z.Codec(dev)
+        streams, sizes = [], []
+        for x in shards:
+            o, nbt = codec.compress(tdev(x), lut)
+            streams.append(o)
+            sizes.append(nbt)
+        torch.cuda.synchronize()
+        sizes_h = [int(s.item()) for s in sizes]
+        ptrs = torch.tensor([s.data_ptr() for s in streams], dtype=torch.int64, device=dev)
+        inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
+        y = torch.empty(n, dtype=torch.int16, device=dev)
+        wsb = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, n, S)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+        def red():
+            z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n, ws.data_ptr(),
+                                             wsb, st_ptr, h), "decompress_reduce")
+        launches_per_step = 1
+        names = ["reduce_kernel"]
+        alg = {"reduce_kernel": sum(sizes_h) + 2 * n}
+        step_input_bytes = 2 * S * n
+
+        def step(k, ev=None):
+            flush.zero_()  # L2 flush (512 MB write), outside the kernel events
+            if ev:
+                ev[0].record(stream)
+            red()
+            if ev:
+                ev[1].record(stream)
+                ev[2].record(stream)
+        cfg_extra = {"n": n, "shards": S, "stream_bytes_total": sum(sizes_h),
+                     "step": "one fused decompress+reduce of S shards",
+                     "l2": "512 MB write between steps flushes L2 (outside kernel events)"}
+
+    # ---- warm-up, then K timed steps ----
+    for k in range(args.warmup):
+        step(k + 1)
+    torch.cuda.synchronize()
+    status.zero_()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(args.warmup + 1 + k, evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(pg, dev)
+    st = int(status.item())
+    if st != 0:
+        raise SystemExit(f"device status {st} ({z.status_string(st)}) during the timed region")
+    k_ms = {names[0]: statistics.mean(e[0].elapsed_time(e[1]) for e in evs)}
+    if len(names) > 1:
+        k_ms[names[1]] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    region_ms = t_start.elapsed_time(t_end)
+    kernel_ms = sum(k_ms.values())
+    ms_per_step = kernel_ms if kind != "roundtrip" else region_ms / args.steps
+    ms_per_step = max_over_ranks(pg, ms_per_step, dev)
+    value = world * step_input_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if kind == "roundtrip" and not args.no_e2e:
+        hx = torch.from_numpy(host.view(np.int16)).pin_memory()
+        hy = torch.empty(n, dtype=torch.int16).pin_memory()
+        hnb = torch.empty(1, dtype=torch.int64).pin_memory()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+
+        def e2e_step():
+            xs[0].copy_(hx, non_blocking=True)
+            comp(0)
+            decomp(0)
+            hy.copy_(y, non_blocking=True)
+            hnb.copy_(nbs[0], non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = ev0.elapsed_time(ev1) / args.steps
+        e2e_ms = max_over_ranks(pg, e2e_ms, dev)
+        assert np.array_equal(hy.numpy().view(np.uint16), host), "e2e round trip not bit-exact"
+        e2e = {"value": round(world * 2 * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 8,
+               "path": "pinned host -> H2D -> zccl_compress -> zccl_decompress -> D2H"}
+
+    if rank != 0:
+        return
+    peak, peak_kind = hbm_peak()
+    dom = max(k_ms, key=k_ms.get)
+    achieved = alg[dom] / (k_ms[dom] * 1e-3) / 1e9
+    kernels = {}
+    for nm in names:
+        a = alg[nm] / (k_ms[nm] * 1e-3) / 1e9
+        inp = (step_input_bytes / len(names)) / (k_ms[nm] * 1e-3) / 1e9
+        kernels[nm] = {"ms": round(k_ms[nm], 4), "bf16_input_gbs": round(inp, 2),
+                       "algorithmic_bytes": alg[nm], "achieved_gbs": round(a, 2),
+                       "frac_of_" + peak_kind: round(a / peak, 4)}
+    line = {
+        "metric": "compress/decompress GB/s of BF16 input",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": workload_desc(args.workload), **cfg_extra,
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": ncu_traffic(dom, args.workload),
+                     "algorithmic_bytes_per_launch": alg[dom]},
+        "kernels": kernels,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

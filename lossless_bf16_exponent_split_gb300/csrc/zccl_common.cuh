@@ -222,11 +222,13 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* scratch, T* total)
 
 // ---- decoupled look-back ----------------------------------------------------
 // Called by one full warp for work unit `unit` whose scan segment starts at
-// `seg_first`.  Publishes `agg` (this unit's escape count), waits -- with a
-// bound -- for predecessors' flags and returns the exclusive prefix in
-// *exclusive.  Predecessors always hold lower tickets, so they are running
-// or done and every wait ends; a wait that still runs out (or a poisoned
-// predecessor) marks this unit poisoned and returns ZCCL_ERR_TIMEOUT.
+// `seg_first`.  Publishes `agg` (the unit's escape count), reads predecessors'
+// flags 32*kPerLane at a time (each lane kPerLane of them, bounded waits) and
+// returns the exclusive prefix in *exclusive.  Units are taken by ticket, so
+// every predecessor is held by a CTA that is running or done and every wait
+// ends; a wait that still runs out (or a poisoned predecessor) marks this
+// unit poisoned and returns ZCCL_ERR_TIMEOUT.
+template <int kPerLane>
 __device__ inline uint32_t lookback(uint64_t* flags, uint32_t unit, uint32_t seg_first, uint64_t agg,
                                     uint32_t tag, uint64_t* exclusive)
 {
@@ -241,45 +243,75 @@ __device__ inline uint32_t lookback(uint64_t* flags, uint32_t unit, uint32_t seg
     int64_t base = (int64_t)unit - 1;
     const uint64_t t0 = globaltimer();
     for (;;) {
-        const int64_t idx = base - lane;
-        uint64_t state = kFlagPrefix, val = 0;
+        uint64_t state[kPerLane], val[kPerLane];
         bool timed_out = false;
-        if (idx >= (int64_t)seg_first) {
-            for (uint32_t it = 0;; ++it) {
-                const uint64_t f = ld_acquire(&flags[idx]);
-                if ((uint32_t)((f >> 40) & 0x3FFFFF) == tag && (f >> 62) != 0) {
-                    state = f >> 62;
-                    val = f & kValueMask;
-                    break;
-                }
-                if ((it & 31) == 31) {
-                    if (globaltimer() - t0 > kSpinTimeoutNs) {
-                        timed_out = true;
+#pragma unroll
+        for (int q = 0; q < kPerLane; ++q) {
+            const int64_t idx = base - lane - 32 * q;  // distance lane + 32 q
+            state[q] = kFlagPrefix;
+            val[q] = 0;
+            if (idx >= (int64_t)seg_first && !timed_out) {
+                for (uint32_t it = 0;; ++it) {
+                    const uint64_t f = ld_acquire(&flags[idx]);
+                    if ((uint32_t)((f >> 40) & 0x3FFFFF) == tag && (f >> 62) != 0) {
+                        state[q] = f >> 62;
+                        val[q] = f & kValueMask;
                         break;
                     }
-                    __nanosleep(64);
+                    if ((it & 31) == 31) {
+                        if (globaltimer() - t0 > kSpinTimeoutNs) {
+                            timed_out = true;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
                 }
             }
         }
-        const uint32_t bad = __ballot_sync(0xffffffffu, timed_out || state == kFlagPoison);
-        if (bad) {
+        bool bad_lane = timed_out;
+#pragma unroll
+        for (int q = 0; q < kPerLane; ++q) bad_lane = bad_lane || state[q] == kFlagPoison;
+        if (__ballot_sync(0xffffffffu, bad_lane)) {
             if (lane == 0) st_release(&flags[unit], make_flag(kFlagPoison, tag, 0));
             *exclusive = 0;
             return ZCCL_ERR_TIMEOUT;
         }
-        const uint32_t pm = __ballot_sync(0xffffffffu, state == kFlagPrefix);
-        if (pm) {
-            const int first = __ffs(pm) - 1;
-            excl += warp_sum_u64(lane <= first ? val : 0);
-            break;
+        // nearest PREFIX: smallest distance lane + 32 q
+        bool found = false;
+        uint64_t part = 0;
+#pragma unroll
+        for (int q = 0; q < kPerLane; ++q) {
+            if (found) break;
+            const uint32_t pm = __ballot_sync(0xffffffffu, state[q] == kFlagPrefix);
+            if (pm) {
+                const int first = __ffs(pm) - 1;
+                part += lane <= first ? val[q] : 0;
+                found = true;
+            } else {
+                part += val[q];
+            }
         }
-        excl += warp_sum_u64(val);
-        base -= 32;
+        excl += warp_sum_u64(part);
+        if (found) break;
+        base -= 32 * kPerLane;
     }
     if (lane == 0) st_release(&flags[unit], make_flag(kFlagPrefix, tag, excl + agg));
     *exclusive = excl;
     return ZCCL_OK;
 }
+
+// ---- programmatic dependent launch -------------------------------------------
+// The first kernel of a pair lets the second launch once its CTAs are done
+// with their main work; the second waits for the first's completion (and its
+// memory) before reading what the first wrote.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Chunks per scan range of the small look-back kernels.
+constexpr uint32_t kRangeChunks = 32;
 
 // ---- end of a call ----------------------------------------------------------
 // Every CTA calls this once, last, with all its threads.  The CTA that

@@ -1,6 +1,6 @@
-// zccl_compress.cu -- compress kernel: split, remap, code planes, escape
-// counts, single-pass scan and zero-point compaction, for one stream or for a
-// batch of ragged segments in a single launch.
+// zccl_compress.cu -- compression: split, remap, code planes, escape counts,
+// device-wide exclusive scan and zero-point compaction, for one stream or
+// for a batch of ragged segments.
 //
 // Page: "ZipCCL: Efficient Lossless Data Compression of Communication
 // Collectives for Accelerating LLM Training", technical summary 2.B (split
@@ -10,18 +10,25 @@
 // three independent 1-bit arrays; asynchronous global->shared copies with
 // double buffering) and 2.D (static/dynamic MoE parts -> batched segments).
 //
-// GB300 design.  A persistent grid of 128-thread CTAs takes 4096-element
-// chunks by ticket.  Each chunk's 8 KB of BF16 arrives in shared memory by a
-// TMA bulk copy (cp.async.bulk + mbarrier), double-buffered so the next
-// chunk streams in while this one is coded.  Each thread codes 8 consecutive
-// elements per step from one 16-byte shared load: byte permutes give the
-// sign-mantissa bytes; a 256-entry shared table gives each exponent's three
-// code bits pre-spread one byte apart, accumulated into one word whose bytes
-// are the three plane bytes.  The coded block (sign-mantissa bytes + planes)
-// is assembled in shared memory and leaves by one bulk store.  Escape counts
-// come from popc over the plane words; a decoupled look-back (bounded waits)
-// gives the chunk's zero-point offset, and the escapes are written straight
-// to their compacted place: one pass over HBM, no escape scratch.
+// GB300 design: two kernels back to back on the caller's stream, the second
+// started by programmatic dependent launch so its launch overlaps the
+// first's tail.
+//
+//  compress_blocks_kernel  streams the input once.  A persistent grid of
+//    128-thread CTAs walks the 4096-element chunks; each chunk's 8 KB arrives
+//    in shared memory by a TMA bulk copy, double-buffered so the next chunk
+//    lands while this one is coded.  A thread codes 8 consecutive elements
+//    from one 16-byte shared load: byte permutes give the sign-mantissa
+//    bytes, a 256-entry shared table gives each exponent's three code bits
+//    pre-spread one byte apart, accumulated into one word whose bytes are the
+//    three plane bytes.  The coded block leaves by one bulk store.  popc over
+//    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
+//    chunk into a staging slot of the workspace and the count is recorded.
+//    No CTA ever waits for another.
+//  compress_place_kernel  scans the per-chunk counts in ranges of 32 chunks
+//    (ticket-ordered decoupled look-back, 128 flags read per round, bounded
+//    waits), copies each chunk's staged escapes to its place in the
+//    zero-point array, and finishes each stream (header, padding, size).
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -34,22 +41,6 @@ namespace {
 constexpr int kThreads = 128;
 constexpr uint32_t kInBytes = kChunk * 2;  // 8192
 
-struct __align__(16) CompressSmem {
-    uint8_t in[2][kInBytes];       // double-buffered BF16 input chunk
-    uint8_t blk[kBlockBytes];      // coded block being assembled
-    uint32_t code_bits[256];       // exponent -> b0 | b1 << 8 | b2 << 16
-    uint64_t bar[2];               // one mbarrier per input buffer
-    uint32_t scan[kThreads / 32];
-    uint64_t scan64[kThreads / 32];
-    uint64_t total_units;
-    uint32_t ticket_next;
-    uint32_t gen;
-    uint32_t flag;
-    uint32_t lb_status;
-    uint64_t lb_prefix;
-    uint32_t abort;
-};
-
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
 // Why a batched segment descriptor cannot be compressed (0 = it can).
@@ -61,84 +52,94 @@ __device__ __forceinline__ uint32_t segment_error(const zccl_segment_t& d)
     return 0;
 }
 
-// Segment of `unit`: largest s with seg_start[s] <= unit (seg_start has
-// n_segs + 1 entries, non-decreasing).
-__device__ __forceinline__ uint32_t find_segment(const uint32_t* seg_start, uint32_t n_segs, uint32_t unit)
+__device__ __forceinline__ zccl_segment_t seg_get(const CompressArgs& a, uint32_t s)
 {
-    uint32_t lo = 0, hi = n_segs;  // answer in [lo, hi)
+    return a.segs == nullptr ? a.single : a.segs[s];
+}
+
+// Largest s with start[s] <= x (start has n_segs + 1 non-decreasing entries).
+__device__ __forceinline__ uint32_t find_segment(const uint32_t* start, uint32_t n_segs, uint32_t x)
+{
+    uint32_t lo = 0, hi = n_segs;
     while (hi - lo > 1) {
-        uint32_t mid = (lo + hi) >> 1;
-        if (seg_start[mid] <= unit) lo = mid; else hi = mid;
+        const uint32_t mid = (lo + hi) >> 1;
+        if (start[mid] <= x) lo = mid; else hi = mid;
     }
     return lo;
 }
 
-__device__ __forceinline__ void seg_get(const CompressArgs& a, uint32_t s, const uint16_t*& in, uint64_t& n,
-                                        uint8_t*& out)
+// Per-segment chunk (and range) starts in shared memory: ustart[s] = first
+// global chunk of segment s, rstart[s] = first global range.  Invalid
+// segments get no chunks.  Returns the totals through *units, *ranges.
+// All threads; contains barriers.
+__device__ void segment_table(const CompressArgs& a, uint32_t* ustart, uint32_t* rstart, uint64_t* scan64,
+                              uint64_t* units_total, uint64_t* ranges_total)
 {
-    if (a.segs == nullptr) {
-        in = a.single.in;
-        n = a.single.n;
-        out = (uint8_t*)a.single.out;
-    } else {
-        zccl_segment_t d = a.segs[s];
-        in = d.in;
-        n = d.n;
-        out = (uint8_t*)d.out;
+    uint64_t run_u = 0, run_r = 0;
+    for (uint32_t base = 0; base < a.n_segs; base += kThreads) {
+        const uint32_t s = base + threadIdx.x;
+        uint64_t u = 0;
+        if (s < a.n_segs) {
+            const zccl_segment_t d = seg_get(a, s);
+            if (a.segs == nullptr || segment_error(d) == 0) u = units_of(d.n);
+        }
+        const uint64_t r = (u + kRangeChunks - 1) / kRangeChunks;
+        uint64_t tot_u, tot_r;
+        const uint64_t ex_u = block_exclusive_scan<kThreads, uint64_t>(u, scan64, &tot_u);
+        const uint64_t ex_r = block_exclusive_scan<kThreads, uint64_t>(r, scan64, &tot_r);
+        if (s < a.n_segs) {
+            ustart[s] = (uint32_t)(run_u + ex_u);  // used only when the totals are in range
+            rstart[s] = (uint32_t)(run_r + ex_r);
+        }
+        run_u += tot_u;
+        run_r += tot_r;
     }
+    if (threadIdx.x == 0) {
+        ustart[a.n_segs] = (uint32_t)run_u;
+        rstart[a.n_segs] = (uint32_t)run_r;
+    }
+    *units_total = run_u;
+    *ranges_total = run_r;
+    __syncthreads();
 }
 
-// Queue the bulk load of `unit` into buffer `buf` (thread 0 only).
-__device__ __forceinline__ void issue_load(const CompressArgs& a, const uint32_t* seg_start, CompressSmem& sm,
-                                           uint32_t unit, int buf)
+// ============================================================================
+// Kernel 1: code blocks, count and stage escapes
+// ============================================================================
+struct __align__(16) BlocksSmem {
+    uint8_t in[2][kInBytes];   // double-buffered BF16 input chunk
+    uint8_t blk[kBlockBytes];  // coded block being assembled
+    uint32_t code_bits[256];   // exponent -> b0 | b1 << 8 | b2 << 16
+    uint64_t bar[2];
+    uint64_t scan64[kThreads / 32];
+    uint32_t scan[kThreads / 32];
+    uint32_t abort;
+};
+
+__device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, BlocksSmem& sm,
+                                                 uint32_t c, int buf)
 {
-    const uint32_t s = find_segment(seg_start, a.n_segs, unit);
-    const uint16_t* in;
-    uint64_t n;
-    uint8_t* out;
-    seg_get(a, s, in, n, out);
-    const uint64_t c = unit - seg_start[s];
-    const uint64_t first = c * kChunk;
-    const uint32_t valid = (uint32_t)umin64(kChunk, n - first);
-    const uint32_t bytes = (valid * 2) & ~15u;  // whole 16-byte pieces
+    const uint32_t s = find_segment(ustart, a.n_segs, c);
+    const zccl_segment_t d = seg_get(a, s);
+    const uint64_t first = (uint64_t)(c - ustart[s]) * kChunk;
+    const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
+    const uint32_t bytes = (valid * 2) & ~15u;  // whole 16-byte pieces; the rest by plain loads
     if (bytes) {
         mbar_arrive_expect_tx(&sm.bar[buf], bytes);
-        bulk_g2s(sm.in[buf], in + first, bytes, &sm.bar[buf]);
+        bulk_g2s(sm.in[buf], d.in + first, bytes, &sm.bar[buf]);
     } else {
         mbar_arrive(&sm.bar[buf]);
     }
 }
 
-// Header of a finished stream (32 threads of one warp write 4 bytes each).
-__device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t n_esc, const uint8_t* lut,
-                                             int lane)
-{
-    uint32_t w = 0;
-    const uint64_t zp = zp_offset_of(n);
-    switch (lane) {
-        case 0: w = kMagic; break;
-        case 1: w = kVersion | (kLog2Chunk << 16); break;
-        case 2: w = (uint32_t)n; break;
-        case 3: w = (uint32_t)(n >> 32); break;
-        case 4: w = (uint32_t)n_esc; break;
-        case 5: w = (uint32_t)(n_esc >> 32); break;
-        case 6: w = lut[0] | (lut[1] << 8) | (lut[2] << 16) | ((uint32_t)lut[3] << 24); break;
-        case 7: w = lut[4] | (lut[5] << 8) | (lut[6] << 16); break;
-        case 8: w = (uint32_t)zp; break;
-        case 9: w = (uint32_t)(zp >> 32); break;
-        default: w = 0;
-    }
-    reinterpret_cast<uint32_t*>(out)[lane] = w;
-}
-
-__global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a)
+__global__ void __launch_bounds__(kThreads) compress_blocks_kernel(const CompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    CompressSmem& sm = *reinterpret_cast<CompressSmem*>(smem_raw);
-    uint32_t* seg_start = reinterpret_cast<uint32_t*>(smem_raw + sizeof(CompressSmem));
+    BlocksSmem& sm = *reinterpret_cast<BlocksSmem*>(smem_raw);
+    uint32_t* ustart = reinterpret_cast<uint32_t*>(smem_raw + sizeof(BlocksSmem));
+    uint32_t* rstart = ustart + a.n_segs + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // ---- prologue: code table, segment table, barriers, generation ----
     for (int e = tid; e < 256; e += kThreads) {
         uint32_t c = 0;
 #pragma unroll
@@ -146,104 +147,42 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (a.lut[r] == e) c = r + 1;
         sm.code_bits[e] = (c & 1) | (((c >> 1) & 1) << 8) | (((c >> 2) & 1) << 16);
     }
-    // units per segment (invalid segments get none), then an exclusive scan
-    uint64_t running = 0;
-    for (uint32_t base = 0; base < a.n_segs; base += kThreads) {
-        const uint32_t s = base + tid;
-        uint64_t units = 0;
-        if (s < a.n_segs) {
-            if (a.segs == nullptr) {
-                units = units_of(a.single.n);
-            } else {
-                const zccl_segment_t d = a.segs[s];
-                const uint32_t bad = segment_error(d);
-                if (bad) {
-                    if (blockIdx.x == 0) {
-                        report(a.status, bad);
-                        a.out_bytes[s] = 0;
-                    }
-                } else {
-                    units = units_of(d.n);
-                }
-            }
-        }
-        uint64_t total;
-        const uint64_t ex = block_exclusive_scan<kThreads, uint64_t>(units, sm.scan64, &total);
-        if (s < a.n_segs) seg_start[s] = (uint32_t)(running + ex);  // used only if in range
-        running += total;
+    uint64_t total64, ranges64;
+    segment_table(a, ustart, rstart, sm.scan64, &total64, &ranges64);
+    if (total64 > a.max_units) {  // reported by the placement kernel
+        pdl_launch_dependents();
+        return;
     }
+    const uint32_t total = (uint32_t)total64;
     if (tid == 0) {
-        seg_start[a.n_segs] = (uint32_t)running;
-        sm.total_units = running;
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
-        sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
         sm.abort = 0;
+        if (blockIdx.x < total) issue_chunk_load(a, ustart, sm, blockIdx.x, 0);
     }
     __syncthreads();
-    const uint32_t tag = tag_of_gen(sm.gen);
-    if (sm.total_units > a.max_units) {
-        if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
-        finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
-        return;
-    }
-    const uint32_t total_units = (uint32_t)sm.total_units;
-    // empty, valid segments: header only (CTA 0)
-    if (blockIdx.x == 0) {
-        for (uint32_t s = warp; s < a.n_segs; s += kThreads / 32) {
-            if (seg_start[s + 1] != seg_start[s]) continue;
-            const uint16_t* in;
-            uint64_t n;
-            uint8_t* out;
-            seg_get(a, s, in, n, out);
-            if (n != 0) continue;                                     // skipped: invalid
-            if (a.segs != nullptr && segment_error(a.segs[s])) continue;  // skipped: invalid
-            write_header(out, 0, 0, a.lut, lane);
-            if (lane == 0) a.out_bytes[s] = kHeaderBytes;
-        }
-    }
 
-    // ---- main loop over chunk tickets ----
-    if (tid == 0) {
-        const uint32_t t = atomicAdd(&a.ctrl->ticket, 1u);
-        sm.ticket_next = t;
-        if (t < total_units) issue_load(a, seg_start, sm, t, 0);
-    }
-    __syncthreads();
-    uint32_t cur = sm.ticket_next;
     uint32_t k = 0;
-    while (cur < total_units) {
+    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
         const int buf = k & 1;
-        if (tid == 0) {
-            const uint32_t t = atomicAdd(&a.ctrl->ticket, 1u);
-            sm.ticket_next = t;
-            if (t < total_units) issue_load(a, seg_start, sm, t, buf ^ 1);
-        }
-        const uint32_t s = find_segment(seg_start, a.n_segs, cur);
-        const uint16_t* in;
-        uint64_t n;
-        uint8_t* out;
-        seg_get(a, s, in, n, out);
-        const uint32_t c = cur - seg_start[s];
-        const uint64_t first = (uint64_t)c * kChunk;
-        const uint32_t valid = (uint32_t)umin64(kChunk, n - first);
+        if (tid == 0 && c + gridDim.x < total) issue_chunk_load(a, ustart, sm, c + gridDim.x, buf ^ 1);
+        const uint32_t s = find_segment(ustart, a.n_segs, c);
+        const zccl_segment_t d = seg_get(a, s);
+        const uint32_t cl = c - ustart[s];
+        const uint64_t first = (uint64_t)cl * kChunk;
+        const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
         const uint32_t L = slots_of(valid);
 
         if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
         if (valid < kChunk) {  // tail: the last < 8 elements come by plain loads
-            const uint32_t done = ((valid * 2) & ~15u) / 2;
+            const uint32_t done = valid & ~7u;
             if (tid < (int)(valid - done))
-                reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = in[first + done + tid];
+                reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
         }
         __syncthreads();
-        if (sm.abort) {  // a bulk load never landed: poison this chunk and the prefetched one
-            if (tid == 0) {
-                report(a.status, ZCCL_ERR_TIMEOUT);
-                st_release(&a.flags[cur], make_flag(kFlagPoison, tag, 0));
-                if (sm.ticket_next < total_units)
-                    st_release(&a.flags[sm.ticket_next], make_flag(kFlagPoison, tag, 0));
-            }
+        if (sm.abort) {  // a bulk load never landed (bounded wait ran out)
+            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
             break;
         }
 
@@ -258,14 +197,11 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (e0 + 8 > valid) {
                 const uint32_t nv = valid > e0 ? valid - e0 : 0;  // 0..7
                 keep = (1u << nv) - 1u;
-                uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t m = ((keep >> (2 * q)) & 1 ? 0x0000FFFFu : 0u) |
-                                       ((keep >> (2 * q + 1)) & 1 ? 0xFFFF0000u : 0u);
-                    w[q] &= m;
-                }
-                v = make_uint4(w[0], w[1], w[2], w[3]);
+                const uint32_t m0 = (keep & 1 ? 0x0000FFFFu : 0u) | (keep & 2 ? 0xFFFF0000u : 0u);
+                const uint32_t m1 = (keep & 4 ? 0x0000FFFFu : 0u) | (keep & 8 ? 0xFFFF0000u : 0u);
+                const uint32_t m2 = (keep & 16 ? 0x0000FFFFu : 0u) | (keep & 32 ? 0xFFFF0000u : 0u);
+                const uint32_t m3 = (keep & 64 ? 0x0000FFFFu : 0u) | (keep & 128 ? 0xFFFF0000u : 0u);
+                v = make_uint4(v.x & m0, v.y & m1, v.z & m2, v.w & m3);
             }
             // sign-mantissa bytes: (hi & 0x80) | (lo & 0x7F) for 4 elements at once
             const uint32_t lo01 = __byte_perm(v.x, v.y, 0x6420), hi01 = __byte_perm(v.x, v.y, 0x7531);
@@ -291,11 +227,11 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(out + kHeaderBytes + (uint64_t)c * kBlockBytes, sm.blk, L * 11 / 8);
+            bulk_s2g((uint8_t*)d.out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
             bulk_commit();
         }
 
-        // ---- escape words, counts, block scan ----
+        // ---- escapes: words from the planes, chunk-local compaction ----
         uint32_t esc = 0;
         if (tid < (int)(L / 32)) {
             const uint32_t* pw = reinterpret_cast<const uint32_t*>(sm.blk + L);
@@ -307,11 +243,122 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         }
         uint32_t agg;
         const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+        uint8_t* dst = a.stage + (uint64_t)c * kChunk + excl;
+        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(src);
+        uint32_t m = esc, j = 0;
+        while (m) {
+            const uint32_t b = __ffs(m) - 1;
+            m &= m - 1;
+            dst[j++] = (uint8_t)(x16[32u * tid + b] >> 7);
+        }
+        if (tid == 0) {
+            a.counts[c] = agg;
+            bulk_wait_read0();
+        }
+        __syncthreads();
+    }
+    if (tid == 0) bulk_wait0();
+    pdl_launch_dependents();
+}
 
-        // ---- zero-point offset of this chunk: decoupled look-back ----
+// ============================================================================
+// Kernel 2: scan counts, place escapes, finish streams
+// ============================================================================
+struct __align__(16) PlaceSmem {
+    uint64_t scan64[kThreads / 32];
+    uint32_t scan[kThreads / 32];
+    uint32_t cnt[kRangeChunks];
+    uint32_t excl[kRangeChunks];
+    uint32_t ticket;
+    uint32_t gen;
+    uint32_t flag;
+    uint32_t lb_status;
+    uint64_t lb_prefix;
+};
+
+// Header of a finished stream (the 32 lanes of one warp write 4 bytes each).
+__device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t n_esc, const uint8_t* lut,
+                                             int lane)
+{
+    uint32_t w = 0;
+    const uint64_t zp = zp_offset_of(n);
+    switch (lane) {
+        case 0: w = kMagic; break;
+        case 1: w = kVersion | (kLog2Chunk << 16); break;
+        case 2: w = (uint32_t)n; break;
+        case 3: w = (uint32_t)(n >> 32); break;
+        case 4: w = (uint32_t)n_esc; break;
+        case 5: w = (uint32_t)(n_esc >> 32); break;
+        case 6: w = lut[0] | (lut[1] << 8) | (lut[2] << 16) | ((uint32_t)lut[3] << 24); break;
+        case 7: w = lut[4] | (lut[5] << 8) | (lut[6] << 16); break;
+        case 8: w = (uint32_t)zp; break;
+        case 9: w = (uint32_t)(zp >> 32); break;
+        default: w = 0;
+    }
+    reinterpret_cast<uint32_t*>(out)[lane] = w;
+}
+
+__global__ void __launch_bounds__(kThreads) compress_place_kernel(const CompressArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    PlaceSmem& sm = *reinterpret_cast<PlaceSmem*>(smem_raw);
+    uint32_t* ustart = reinterpret_cast<uint32_t*>(smem_raw + sizeof(PlaceSmem));
+    uint32_t* rstart = ustart + a.n_segs + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    pdl_wait();  // counts and staged escapes of the blocks kernel
+    uint64_t total_units, total_ranges;
+    segment_table(a, ustart, rstart, sm.scan64, &total_units, &total_ranges);
+    if (tid == 0) sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
+    __syncthreads();
+    const uint32_t tag = tag_of_gen(sm.gen);
+    if (blockIdx.x == 0 && a.segs != nullptr) {
+        for (uint32_t s = tid; s < a.n_segs; s += kThreads) {
+            const uint32_t bad = segment_error(a.segs[s]);
+            if (bad) {
+                report(a.status, bad);
+                a.out_bytes[s] = 0;
+            }
+        }
+    }
+    if (total_units > a.max_units || total_ranges > a.max_ranges) {
+        if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
+        finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
+        return;
+    }
+    // empty, valid segments: header only (CTA 0)
+    if (blockIdx.x == 0) {
+        for (uint32_t s = warp; s < a.n_segs; s += kThreads / 32) {
+            const zccl_segment_t d = seg_get(a, s);
+            if (d.n != 0 || (a.segs != nullptr && segment_error(d))) continue;
+            write_header((uint8_t*)d.out, 0, 0, a.lut, lane);
+            if (lane == 0) a.out_bytes[s] = kHeaderBytes;
+        }
+    }
+
+    const uint32_t nr = (uint32_t)total_ranges;
+    for (;;) {
+        if (tid == 0) sm.ticket = atomicAdd(&a.ctrl->ticket, 1u);
+        __syncthreads();
+        const uint32_t r = sm.ticket;
+        if (r >= nr) break;
+        const uint32_t s = find_segment(rstart, a.n_segs, r);
+        const zccl_segment_t d = seg_get(a, s);
+        const uint32_t q = r - rstart[s];
+        const uint32_t seg_units = (uint32_t)units_of(d.n);
+        const uint32_t c0 = q * kRangeChunks;                       // first chunk, segment-local
+        const uint32_t nch = min(kRangeChunks, seg_units - c0);
+        const uint32_t g0 = ustart[s] + c0;                          // first chunk, global
+        const uint32_t cnt = tid < (int)nch ? a.counts[g0 + tid] : 0u;
+        uint32_t agg;
+        const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
+        if (tid < (int)kRangeChunks) {
+            sm.cnt[tid] = cnt;
+            sm.excl[tid] = ex;
+        }
         if (warp == 0) {
             uint64_t pre;
-            const uint32_t st = lookback(a.flags, cur, seg_start[s], agg, tag, &pre);
+            const uint32_t st = lookback<4>(a.flags, r, rstart[s], agg, tag, &pre);
             if (lane == 0) {
                 sm.lb_status = st;
                 sm.lb_prefix = pre;
@@ -322,63 +369,56 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (tid == 0) report(a.status, sm.lb_status);
         } else {
             const uint64_t P = sm.lb_prefix;
-            const uint64_t zp = zp_offset_of(n);
-            // compacted escapes, element order
-            uint8_t* dst = out + zp + P + excl;
-            const uint16_t* x16 = reinterpret_cast<const uint16_t*>(src);
-            uint32_t m = esc, j = 0;
-            while (m) {
-                const uint32_t b = __ffs(m) - 1;
-                m &= m - 1;
-                dst[j++] = (uint8_t)(x16[32u * tid + b] >> 7);
+            const uint64_t zp = zp_offset_of(d.n);
+            uint8_t* out = (uint8_t*)d.out;
+            for (uint32_t i = warp; i < nch; i += kThreads / 32) {
+                const uint8_t* from = a.stage + (uint64_t)(g0 + i) * kChunk;
+                uint8_t* to = out + zp + P + sm.excl[i];
+                for (uint32_t j = lane; j < sm.cnt[i]; j += 32) to[j] = from[j];
             }
-            // last chunk of the segment: header, zero padding, size
-            if (c + 1 == seg_start[s + 1] - seg_start[s]) {
+            if (c0 + nch == seg_units) {  // last range: header, zero padding, size
                 const uint64_t n_esc = P + agg;
                 const uint64_t pad_end = round_up(n_esc, 128);
                 for (uint64_t b = n_esc + tid; b < pad_end; b += kThreads) out[zp + b] = 0;
-                if (warp == 1) write_header(out, n, n_esc, a.lut, lane);
+                if (warp == 1) write_header(out, d.n, n_esc, a.lut, lane);
                 if (tid == 0) a.out_bytes[s] = zp + pad_end;
             }
         }
-        if (tid == 0) bulk_wait_read0();
         __syncthreads();
-        cur = sm.ticket_next;
-        ++k;
-    }
-    if (tid == 0) bulk_wait0();
-    // a buffer may still have a load in flight if the loop stopped early
-    // (abort): wait for it, bounded, before the CTA's smem is released
-    if (tid == 0 && cur < total_units && sm.ticket_next < total_units) {
-        mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);
     }
     finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
 }
 
-}  // namespace
-
-size_t compress_smem_bytes(uint32_t n_segs) { return sizeof(CompressSmem) + 4ull * (n_segs + 1); }
-
-cudaError_t launch_compress(const CompressArgs& a, uint32_t grid, cudaStream_t stream)
-{
-    const size_t smem = compress_smem_bytes(a.n_segs);
-    cudaError_t e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    compress_kernel<<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
-}
-
-int compress_ctas_per_sm(uint32_t n_segs)
+template <typename K>
+int occupancy(K kernel, size_t smem)
 {
     int blocks = 0;
-    const size_t smem = compress_smem_bytes(n_segs);
-    if (cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, compress_kernel, kThreads, smem) != cudaSuccess)
-        return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess) return 1;
     return blocks > 0 ? blocks : 1;
 }
+
+}  // namespace
+
+size_t compress_smem_bytes(uint32_t n_segs) { return sizeof(BlocksSmem) + 8ull * (n_segs + 1); }
+static size_t place_smem_bytes(uint32_t n_segs) { return sizeof(PlaceSmem) + 8ull * (n_segs + 1); }
+
+cudaError_t launch_compress(const CompressArgs& a, uint32_t grid_blocks, uint32_t grid_place, cudaStream_t stream)
+{
+    const size_t smem1 = compress_smem_bytes(a.n_segs), smem2 = place_smem_bytes(a.n_segs);
+    cudaError_t e = cudaFuncSetAttribute(compress_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(compress_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    if (e != cudaSuccess) return e;
+    compress_blocks_kernel<<<grid_blocks, kThreads, smem1, stream>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_dependent(compress_place_kernel, grid_place, kThreads, smem2, stream, a);
+}
+
+int compress_ctas_per_sm(uint32_t n_segs) { return occupancy(compress_blocks_kernel, compress_smem_bytes(n_segs)); }
+int place_ctas_per_sm(uint32_t n_segs) { return occupancy(compress_place_kernel, place_smem_bytes(n_segs)); }
 
 }  // namespace zccl

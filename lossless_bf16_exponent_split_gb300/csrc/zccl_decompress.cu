@@ -1,6 +1,5 @@
-// zccl_decompress.cu -- decompress kernel: recount escapes from the code
-// planes, single-pass scan (inverse of the encoder's), gather from the
-// zero-point array, rebuild BF16.
+// zccl_decompress.cu -- decompression: inverse scan of the escape counts
+// (recounted from the code planes) and gather from the zero-point array.
 //
 // Page: "ZipCCL: Efficient Lossless Data Compression of Communication
 // Collectives for Accelerating LLM Training", technical summary 2.B (a code
@@ -8,19 +7,29 @@
 // zero-point array) and 2.C (128-byte aligned blocks, three 1-bit code
 // arrays, asynchronous global->shared copies with double buffering).
 //
-// GB300 design.  Persistent 128-thread CTAs take 4096-element chunks by
-// ticket; each chunk block (5632 bytes) arrives by a TMA bulk copy into one
-// of two shared buffers.  popc over ~(p0|p1|p2) gives the chunk's escape
-// count; a decoupled look-back gives its offset into the zero-point array;
-// escaped exponents are scattered into a per-element shared array.  Each
-// thread then rebuilds 8 consecutive elements: the three plane bytes are
-// spread to nibble codes, one byte-permute per 4 elements looks the codes up
-// in the LUT (held in two registers), a second permute makes the escape
-// mask, and byte permutes interleave sign-mantissa and exponent bytes into
-// BF16, stored with one 16-byte write.
+// GB300 design: two kernels, the second started by programmatic dependent
+// launch.
+//
+//  escape_scan_kernel  reads only the code planes (3/8 byte per element).
+//    Each warp counts the escapes of a chunk with 16-byte loads and popc of
+//    ~(p0|p1|p2); ranges of 32 chunks are scanned across the grid by a
+//    ticket-ordered decoupled look-back (128 flags per round, bounded
+//    waits); the result is every chunk's offset into the zero-point array,
+//    plus the total, checked against the header.  It serves S streams at
+//    once for the fused reduction.
+//  decompress_kernel  streams the blocks once: per chunk, one TMA bulk copy
+//    brings the block and a second brings the chunk's run of the zero-point
+//    array (known from the offsets), both completing on one mbarrier,
+//    double-buffered.  Escaped exponents are scattered to their element slots
+//    in shared memory; each thread rebuilds 8 consecutive elements: plane
+//    bytes spread to nibble codes, one byte permute per 4 elements looks the
+//    codes up in the LUT (two registers), another makes the escape mask, and
+//    byte permutes interleave sign-mantissa and exponent bytes into BF16,
+//    stored with one 16-byte write.
 #include <cstdint>
 
 #include "zccl_common.cuh"
+#include "zccl_decode.cuh"
 #include "zccl_internal.h"
 
 namespace zccl {
@@ -29,222 +38,299 @@ namespace {
 
 constexpr int kThreads = 128;
 
-struct __align__(16) DecompressSmem {
-    uint8_t blk[2][kBlockBytes];  // double-buffered chunk blocks
-    uint8_t expo[kChunk];         // escaped exponents at their element slot
-    uint64_t bar[2];
+// ============================================================================
+// Kernel 1: escape offsets from the code planes
+// ============================================================================
+struct __align__(16) ScanSmem {
     uint32_t scan[kThreads / 32];
-    uint32_t ticket_next;
+    uint32_t cnt[kRangeChunks];
+    uint32_t ticket;
     uint32_t gen;
     uint32_t flag;
     uint32_t lb_status;
-    uint32_t abort;
     uint32_t hdr_ok;
-    uint32_t lut_lo, lut_hi;  // byte r+1 = exponent of code r+1; byte 0 = 0
-    uint64_t lb_prefix;
     uint64_t n_esc;
+    uint64_t lb_prefix;
 };
 
-__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
-
-// bit k of an 8-bit value -> bit 4k
-__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x)
+__device__ __forceinline__ const uint8_t* scan_stream(const ScanArgs& a, uint32_t s)
 {
-    x = (x | (x << 12)) & 0x000F000Fu;
-    x = (x | (x << 6)) & 0x03030303u;
-    x = (x | (x << 3)) & 0x11111111u;
-    return x;
+    return a.streams == nullptr ? a.single : reinterpret_cast<const uint8_t*>(a.streams[s]);
+}
+__device__ __forceinline__ uint64_t scan_in_bytes(const ScanArgs& a, uint32_t s)
+{
+    return a.in_bytes_dev == nullptr ? a.in_bytes : a.in_bytes_dev[s];
 }
 
-__device__ __forceinline__ void issue_load(const DecompressArgs& a, DecompressSmem& sm, uint32_t unit, int buf)
+// Escape count of one chunk, by one warp (valid elements only).
+__device__ __forceinline__ uint32_t warp_chunk_escapes(const uint8_t* blk, uint32_t valid)
 {
-    const uint32_t valid = (uint32_t)umin64(kChunk, a.n - (uint64_t)unit * kChunk);
-    const uint32_t bytes = slots_of(valid) * 11 / 8;
-    mbar_arrive_expect_tx(&sm.bar[buf], bytes);
-    bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)unit * kBlockBytes, bytes, &sm.bar[buf]);
-}
-
-// Rebuilds 8 consecutive elements from a chunk block: sign-mantissa bytes,
-// plane bytes pb0..pb2, LUT in two registers, escaped exponents `xe`.
-__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
-                                         uint32_t lut_hi, uint2 xe)
-{
-    const uint32_t N = spread_nibbles(pb0) | (spread_nibbles(pb1) << 1) | (spread_nibbles(pb2) << 2);
-    uint32_t e_lo = __byte_perm(lut_lo, lut_hi, N);
-    uint32_t e_hi = __byte_perm(lut_lo, lut_hi, N >> 16);
-    const uint32_t m_lo = __byte_perm(0xFFu, 0u, N);  // 0xFF where code == 0
-    const uint32_t m_hi = __byte_perm(0xFFu, 0u, N >> 16);
-    e_lo = (e_lo & ~m_lo) | (xe.x & m_lo);
-    e_hi = (e_hi & ~m_hi) | (xe.y & m_hi);
-    const uint32_t lo_a = (smb.x & 0x7F7F7F7Fu) | ((e_lo << 7) & 0x80808080u);
-    const uint32_t hi_a = (smb.x & 0x80808080u) | ((e_lo >> 1) & 0x7F7F7F7Fu);
-    const uint32_t lo_b = (smb.y & 0x7F7F7F7Fu) | ((e_hi << 7) & 0x80808080u);
-    const uint32_t hi_b = (smb.y & 0x80808080u) | ((e_hi >> 1) & 0x7F7F7F7Fu);
-    return make_uint4(__byte_perm(lo_a, hi_a, 0x5140), __byte_perm(lo_a, hi_a, 0x7362),
-                      __byte_perm(lo_b, hi_b, 0x5140), __byte_perm(lo_b, hi_b, 0x7362));
-}
-
-__global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressArgs a)
-{
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    DecompressSmem& sm = *reinterpret_cast<DecompressSmem*>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t total_units = (uint32_t)units_of(a.n);
-
-    if (tid == 0) {
-        // header checks: magic, version, chunk size, n, zp_offset, sizes
-        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
-        const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-        const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-        const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-        bool ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
-                  zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= a.in_bytes;
-        sm.hdr_ok = ok ? 1u : 0u;
-        sm.n_esc = n_esc;
-        sm.lut_lo = h[6] << 8;                     // codes 1..3 in bytes 1..3, byte 0 = 0
-        sm.lut_hi = (h[6] >> 24) | (h[7] << 8);    // codes 4..7
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
-        sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
-        sm.abort = 0;
-    }
-    __syncthreads();
-    const uint32_t tag = tag_of_gen(sm.gen);
-    if (!sm.hdr_ok) {
-        if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-        finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
-        return;
-    }
-    const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
-    const uint64_t n_esc = sm.n_esc;
-    const uint8_t* zp_base = a.in + zp_offset_of(a.n);
-
-    if (tid == 0) {
-        const uint32_t t = atomicAdd(&a.ctrl->ticket, 1u);
-        sm.ticket_next = t;
-        if (t < total_units) issue_load(a, sm, t, 0);
-    }
-    __syncthreads();
-    uint32_t cur = sm.ticket_next;
-    uint32_t k = 0;
-    while (cur < total_units) {
-        const int buf = k & 1;
-        if (tid == 0) {
-            const uint32_t t = atomicAdd(&a.ctrl->ticket, 1u);
-            sm.ticket_next = t;
-            if (t < total_units) issue_load(a, sm, t, buf ^ 1);
-        }
-        const uint64_t first = (uint64_t)cur * kChunk;
-        const uint32_t valid = (uint32_t)umin64(kChunk, a.n - first);
-        const uint32_t L = slots_of(valid);
-        if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
-        __syncthreads();
-        if (sm.abort) {
-            if (tid == 0) {
-                report(a.status, ZCCL_ERR_TIMEOUT);
-                st_release(&a.flags[cur], make_flag(kFlagPoison, tag, 0));
-                if (sm.ticket_next < total_units)
-                    st_release(&a.flags[sm.ticket_next], make_flag(kFlagPoison, tag, 0));
-            }
-            break;
-        }
-        const uint8_t* blk = sm.blk[buf];
-
-        // ---- escape words from the planes, counts, block scan ----
-        uint32_t esc = 0;
-        if (tid < (int)(L / 32)) {
-            const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-            const uint32_t p0 = pw[tid], p1 = pw[L / 32 + tid], p2 = pw[L / 16 + tid];
-            const uint32_t w0 = 32u * tid;
+    const int lane = threadIdx.x & 31;
+    const uint32_t L = slots_of(valid);
+    uint32_t c = 0;
+    if (valid == kChunk) {
+        const uint4 p0 = reinterpret_cast<const uint4*>(blk + kChunk)[lane];
+        const uint4 p1 = reinterpret_cast<const uint4*>(blk + kChunk + kChunk / 8)[lane];
+        const uint4 p2 = reinterpret_cast<const uint4*>(blk + kChunk + kChunk / 4)[lane];
+        c = __popc(~(p0.x | p1.x | p2.x)) + __popc(~(p0.y | p1.y | p2.y)) + __popc(~(p0.z | p1.z | p2.z)) +
+            __popc(~(p0.w | p1.w | p2.w));
+    } else {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+        for (uint32_t w = lane; w < L / 32; w += 32) {
+            const uint32_t w0 = 32u * w;
             const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
                                    : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-            esc = ~(p0 | p1 | p2) & vmask;
+            c += __popc(~(pw[w] | pw[L / 32 + w] | pw[L / 16 + w]) & vmask);
         }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
+}
+
+__global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
+{
+    __shared__ ScanSmem sm;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t units = (uint32_t)units_of(a.n);
+    const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;  // ranges per stream
+    const uint32_t nr = rps * a.S;
+    if (tid == 0) sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
+    __syncthreads();
+    const uint32_t tag = tag_of_gen(sm.gen);
+
+    for (;;) {
+        if (tid == 0) {
+            const uint32_t r = atomicAdd(&a.ctrl->ticket, 1u);
+            sm.ticket = r;
+            if (r < nr) {  // header of this range's stream
+                const uint32_t s = r / rps;
+                const uint8_t* base = scan_stream(a, s);
+                const uint64_t in_bytes = scan_in_bytes(a, s);
+                bool ok = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
+                uint64_t n_esc = 0;
+                if (ok) {
+                    const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
+                    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+                    n_esc = h[4] | ((uint64_t)h[5] << 32);
+                    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+                    ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
+                         zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
+                }
+                sm.hdr_ok = ok;
+                sm.n_esc = n_esc;
+            }
+        }
+        __syncthreads();
+        const uint32_t r = sm.ticket;
+        if (r >= nr) break;
+        const uint32_t s = r / rps, q = r % rps;
+        const uint32_t c0 = q * kRangeChunks;
+        const uint32_t nch = min(kRangeChunks, units - c0);
+        const bool ok = sm.hdr_ok != 0;
+        if (ok) {
+            const uint8_t* base = scan_stream(a, s);
+            for (uint32_t i = warp; i < nch; i += kThreads / 32) {
+                const uint32_t c = c0 + i;
+                const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
+                const uint32_t e = warp_chunk_escapes(base + kHeaderBytes + (uint64_t)c * kBlockBytes, valid);
+                if (lane == 0) sm.cnt[i] = e;
+            }
+        }
+        __syncthreads();
+        const uint32_t cnt = (ok && tid < (int)nch) ? sm.cnt[tid] : 0u;
         uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+        const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
         if (warp == 0) {
             uint64_t pre;
-            const uint32_t st = lookback(a.flags, cur, 0, agg, tag, &pre);
+            const uint32_t st = lookback<4>(a.flags, r, s * rps, agg, tag, &pre);
             if (lane == 0) {
                 sm.lb_status = st;
                 sm.lb_prefix = pre;
             }
         }
         __syncthreads();
-        bool ok = sm.lb_status == ZCCL_OK;
         if (!ok) {
+            if (tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+        } else if (sm.lb_status != ZCCL_OK) {
             if (tid == 0) report(a.status, sm.lb_status);
         } else {
+            uint64_t* off = a.offsets + (uint64_t)s * (units + 1);
             const uint64_t P = sm.lb_prefix;
-            const bool last = cur + 1 == total_units;
-            if (P + agg > n_esc || (last && P + agg != n_esc)) {
-                if (tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-                ok = false;
-            } else {
-                const uint8_t* src = zp_base + P + excl;
-                uint32_t m = esc, j = 0;
-                while (m) {
-                    const uint32_t b = __ffs(m) - 1;
-                    m &= m - 1;
-                    sm.expo[32u * tid + b] = src[j++];
-                }
+            if (tid < (int)nch) off[c0 + tid] = P + ex;
+            if (c0 + nch == units && tid == 0) {
+                off[units] = P + agg;
+                if (P + agg != sm.n_esc) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
             }
         }
         __syncthreads();
-        if (ok) {
+    }
+    pdl_launch_dependents();
+    finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
+}
+
+// ============================================================================
+// Kernel 2: decode
+// ============================================================================
+struct __align__(16) DecodeSmem {
+    uint8_t blk[2][kBlockBytes];   // double-buffered chunk blocks
+    uint8_t zpb[2][kZpBufBytes];   // the chunk's zero-point run (16-byte aligned cover)
+    uint8_t expo[kChunk];          // escaped exponents at their element slot
+    uint64_t bar[2];
+    uint32_t zdelta[2];            // offset of the run's first byte inside zpb
+    uint32_t zcount[2];            // escapes of the chunk (from the offsets)
+    uint32_t scan[kThreads / 32];
+    uint32_t abort;
+    uint32_t hdr_ok;
+    uint32_t lut_lo, lut_hi;
+    uint64_t n_esc;
+};
+
+__device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, int buf)
+{
+    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
+    const uint32_t bytes = slots_of(valid) * 11 / 8;
+    const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1];
+    uint32_t zbytes = 0, delta = 0, cnt = 0;
+    if (o1 >= o0 && o1 <= sm.n_esc && o1 - o0 <= kChunk) {  // offsets checked by the scan kernel too
+        cnt = (uint32_t)(o1 - o0);
+        if (cnt) {
+            const uint64_t lo = zp_offset_of(a.n) + o0, hi = zp_offset_of(a.n) + o1;
+            const uint64_t lo16 = lo & ~15ull, hi16 = round_up(hi, 16);
+            zbytes = (uint32_t)(hi16 - lo16);
+            delta = (uint32_t)(lo - lo16);
+        }
+    } else {
+        report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+    }
+    sm.zdelta[buf] = delta;
+    sm.zcount[buf] = cnt;
+    mbar_arrive_expect_tx(&sm.bar[buf], bytes + zbytes);
+    bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
+    if (zbytes)
+        bulk_g2s(sm.zpb[buf], a.in + ((zp_offset_of(a.n) + o0) & ~15ull), zbytes, &sm.bar[buf]);
+}
+
+__global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t total = (uint32_t)units_of(a.n);
+
+    if (tid == 0) {  // header: the scan kernel checked it too; this CTA needs its LUT
+        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
+        const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+        const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
+        const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+        sm.hdr_ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
+                    zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= a.in_bytes;
+        sm.n_esc = n_esc;
+        sm.lut_lo = h[6] << 8;
+        sm.lut_hi = (h[6] >> 24) | (h[7] << 8);
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+        sm.abort = 0;
+    }
+    pdl_wait();  // offsets of the scan kernel
+    __syncthreads();
+    if (!sm.hdr_ok) return;  // reported by the scan kernel
+    const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
+    if (tid == 0 && blockIdx.x < total) issue_decode_load(a, sm, blockIdx.x, 0);
+
+    uint32_t k = 0;
+    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+        const int buf = k & 1;
+        if (tid == 0 && c + gridDim.x < total) issue_decode_load(a, sm, c + gridDim.x, buf ^ 1);
+        const uint64_t first = (uint64_t)c * kChunk;
+        const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
+        const uint32_t L = slots_of(valid);
+        if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
+        __syncthreads();
+        if (sm.abort) {
+            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
+            break;
+        }
+        const uint8_t* blk = sm.blk[buf];
+        uint32_t esc = 0;
+        if (tid < (int)(L / 32)) {
+            const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+            const uint32_t w0 = 32u * tid;
+            const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
+                                   : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+            esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
+        }
+        uint32_t agg;
+        const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+        const bool good = agg == sm.zcount[buf];
+        if (good) {
+            const uint8_t* src = sm.zpb[buf] + sm.zdelta[buf] + excl;
+            uint32_t m = esc, j = 0;
+            while (m) {
+                const uint32_t b = __ffs(m) - 1;
+                m &= m - 1;
+                sm.expo[32u * tid + b] = src[j++];
+            }
+        } else if (tid == 0) {
+            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+        }
+        __syncthreads();
+        if (good) {
             uint16_t* dst = a.out + first;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
                 if (e0 >= valid) continue;
-                const uint2 smb = *reinterpret_cast<const uint2*>(blk + e0);
-                const uint32_t pb0 = blk[L + (e0 >> 3)];
-                const uint32_t pb1 = blk[L + L / 8 + (e0 >> 3)];
-                const uint32_t pb2 = blk[L + L / 4 + (e0 >> 3)];
-                const uint2 xe = *reinterpret_cast<const uint2*>(sm.expo + e0);
-                const uint4 o = decode8(smb, pb0, pb1, pb2, lut_lo, lut_hi, xe);
+                const uint4 o = decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
+                                        blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
+                                        *reinterpret_cast<const uint2*>(sm.expo + e0));
                 if (e0 + 8 <= valid) {
                     *reinterpret_cast<uint4*>(dst + e0) = o;
                 } else {
-                    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-                    for (uint32_t q = 0; q < valid - e0; ++q)
-                        dst[e0 + q] = (uint16_t)(w[q >> 1] >> (16 * (q & 1)));
+                    store_partial(dst + e0, o, valid - e0);
                 }
             }
         }
         __syncthreads();
-        cur = sm.ticket_next;
-        ++k;
     }
-    if (tid == 0 && cur < total_units && sm.ticket_next < total_units) {
-        mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);
+    // a load still in flight after an early stop: wait for it (bounded)
+    if (tid == 0 && sm.abort) {
+        const uint32_t c = blockIdx.x + k * gridDim.x;
+        if (c + gridDim.x < total) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);
     }
-    finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
+}
+
+template <typename K>
+int occupancy(K kernel, size_t smem)
+{
+    int blocks = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess) return 1;
+    return blocks > 0 ? blocks : 1;
 }
 
 }  // namespace
 
-cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream)
+cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream)
 {
-    const size_t smem = sizeof(DecompressSmem);
-    cudaError_t e = cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    decompress_kernel<<<grid, kThreads, smem, stream>>>(a);
+    escape_scan_kernel<<<grid, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-int decompress_ctas_per_sm()
+cudaError_t launch_decompress(const ScanArgs& s, const DecompressArgs& a, uint32_t grid_scan, uint32_t grid,
+                              cudaStream_t stream)
 {
-    int blocks = 0;
-    const size_t smem = sizeof(DecompressSmem);
-    if (cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decompress_kernel, kThreads, smem) != cudaSuccess)
-        return 1;
-    return blocks > 0 ? blocks : 1;
+    const size_t smem = sizeof(DecodeSmem);
+    cudaError_t e = cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_scan(s, grid_scan, stream);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(decompress_kernel, grid, kThreads, smem, stream, a);
 }
+
+int scan_ctas_per_sm() { return occupancy(escape_scan_kernel, 0); }
+int decompress_ctas_per_sm() { return occupancy(decompress_kernel, sizeof(DecodeSmem)); }
 
 }  // namespace zccl

@@ -27,6 +27,9 @@ struct DeviceInfo {
     int sms = 0;
     int compress_per_sm = 1;
     int compress_per_sm_batched = 1;
+    int place_per_sm = 1;
+    int place_per_sm_batched = 1;
+    int scan_per_sm = 1;
     int decompress_per_sm = 1;
     int reduce_per_sm_small = 1;  // S <= kSmallShards
     int reduce_per_sm_large = 1;  // any S <= ZCCL_MAX_SHARDS
@@ -46,6 +49,9 @@ const DeviceInfo* device_info()
         d.sms = sms > 0 ? sms : 1;
         d.compress_per_sm = compress_ctas_per_sm(1);
         d.compress_per_sm_batched = compress_ctas_per_sm(ZCCL_MAX_SEGMENTS);
+        d.place_per_sm = place_ctas_per_sm(1);
+        d.place_per_sm_batched = place_ctas_per_sm(ZCCL_MAX_SEGMENTS);
+        d.scan_per_sm = scan_ctas_per_sm();
         d.decompress_per_sm = decompress_ctas_per_sm();
         d.reduce_per_sm_small = reduce_ctas_per_sm(kSmallShards);
         d.reduce_per_sm_large = reduce_ctas_per_sm(ZCCL_MAX_SHARDS);
@@ -64,7 +70,42 @@ bool lut_ok(const zccl_lut_t* lut)
     return true;
 }
 
-uint64_t ws_bytes_for_units(uint64_t units) { return round_up(kCtrlBytes + 8 * units, 256); }
+uint64_t ranges_of(uint64_t units) { return (units + kRangeChunks - 1) / kRangeChunks; }
+
+// Compression workspace: control | look-back flag per range | escape count
+// per chunk | a 4096-byte escape staging slot per chunk.
+struct CompressLayout {
+    uint64_t flags, counts, stage, total;
+};
+CompressLayout compress_layout(uint64_t units, uint64_t ranges)
+{
+    CompressLayout l;
+    l.flags = kCtrlBytes;
+    l.counts = l.flags + 8 * ranges;
+    l.stage = round_up(l.counts + 4 * units, 256);
+    l.total = round_up(l.stage + (uint64_t)kChunk * units, 256);
+    return l;
+}
+
+// Decompression / reduction workspace: control | look-back flag per stream
+// and range | zero-point offset per stream and chunk (+ total).
+struct ScanLayout {
+    uint64_t flags, offsets, total;
+};
+ScanLayout scan_layout(uint64_t units, uint64_t S)
+{
+    ScanLayout l;
+    l.flags = kCtrlBytes;
+    l.offsets = round_up(l.flags + 8 * S * ranges_of(units), 16);
+    l.total = round_up(l.offsets + 8 * S * (units + 1), 256);
+    return l;
+}
+
+uint64_t batched_max_units(uint64_t total_n, uint32_t n_segs) { return total_n / kChunk + n_segs; }
+uint64_t batched_max_ranges(uint64_t total_n, uint32_t n_segs)
+{
+    return batched_max_units(total_n, n_segs) / kRangeChunks + n_segs;
+}
 
 uint32_t grid_for(uint64_t units, int per_sm, int sms)
 {
@@ -108,14 +149,16 @@ zccl_status_t zccl_workspace_bytes(int op, uint64_t n, uint32_t k, uint64_t* byt
     if (bytes == nullptr || n >= kMaxElems) return ZCCL_ERR_INVALID_ARG;
     switch (op) {
         case ZCCL_OP_COMPRESS:
-        case ZCCL_OP_DECOMPRESS: *bytes = ws_bytes_for_units(units_of(n)); return ZCCL_OK;
+            *bytes = compress_layout(units_of(n), ranges_of(units_of(n))).total;
+            return ZCCL_OK;
+        case ZCCL_OP_DECOMPRESS: *bytes = scan_layout(units_of(n), 1).total; return ZCCL_OK;
         case ZCCL_OP_COMPRESS_BATCHED:
             if (k == 0 || k > ZCCL_MAX_SEGMENTS) return ZCCL_ERR_INVALID_ARG;
-            *bytes = ws_bytes_for_units(n / kChunk + k);
+            *bytes = compress_layout(batched_max_units(n, k), batched_max_ranges(n, k)).total;
             return ZCCL_OK;
         case ZCCL_OP_DECOMPRESS_REDUCE:
             if (k == 0 || k > ZCCL_MAX_SHARDS) return ZCCL_ERR_INVALID_ARG;
-            *bytes = ws_bytes_for_units(units_of(n) * k);
+            *bytes = scan_layout(units_of(n), k).total;
             return ZCCL_OK;
         default: return ZCCL_ERR_INVALID_ARG;
     }
@@ -136,8 +179,9 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
         !aligned(d_out_bytes, 8) || d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
         return ZCCL_ERR_INVALID_ARG;
     if (out_capacity < zccl_max_compressed_bytes(n)) return ZCCL_ERR_BUFFER_TOO_SMALL;
-    const uint64_t units = units_of(n);
-    if (ws_bytes < ws_bytes_for_units(units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const uint64_t units = units_of(n), ranges = ranges_of(units);
+    const CompressLayout l = compress_layout(units, ranges);
+    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
 
@@ -146,14 +190,19 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
     a.single = zccl_segment_t{d_in, n, d_out, out_capacity};
     a.n_segs = 1;
     a.max_units = (uint32_t)units;
+    a.max_ranges = (uint32_t)ranges;
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
-    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
+    a.n_flag_words = ranges;
+    a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
+    a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
-    const uint32_t grid = grid_for(units, dev->compress_per_sm, dev->sms);
-    return launch_compress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+    return launch_compress(a, grid_for(units, dev->compress_per_sm, dev->sms),
+                           grid_for(ranges, dev->place_per_sm, dev->sms), stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
 }
 
 zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_segs, uint64_t total_n,
@@ -164,8 +213,10 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
         d_segs == nullptr || !aligned(d_segs, 8) || d_out_bytes == nullptr || !aligned(d_out_bytes, 8) ||
         d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
         return ZCCL_ERR_INVALID_ARG;
-    const uint64_t max_units = total_n / kChunk + n_segs;
-    if (ws_bytes < ws_bytes_for_units(max_units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const uint64_t max_units = batched_max_units(total_n, n_segs);
+    const uint64_t max_ranges = batched_max_ranges(total_n, n_segs);
+    const CompressLayout l = compress_layout(max_units, max_ranges);
+    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
 
@@ -173,14 +224,19 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     a.segs = d_segs;
     a.n_segs = n_segs;
     a.max_units = (uint32_t)max_units;
+    a.max_ranges = (uint32_t)max_ranges;
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
-    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
+    a.n_flag_words = max_ranges;
+    a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
+    a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
-    const uint32_t grid = grid_for(max_units, dev->compress_per_sm_batched, dev->sms);
-    return launch_compress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+    return launch_compress(a, grid_for(max_units, dev->compress_per_sm_batched, dev->sms),
+                           grid_for(max_ranges, dev->place_per_sm_batched, dev->sms), stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
 }
 
 zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n, void* d_ws,
@@ -191,21 +247,32 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
         return ZCCL_ERR_INVALID_ARG;
     if (in_bytes < zp_offset_of(n)) return ZCCL_ERR_INVALID_ARG;
     const uint64_t units = units_of(n);
-    if (ws_bytes < ws_bytes_for_units(units)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const ScanLayout l = scan_layout(units, 1);
+    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
 
+    ScanArgs sc{};
+    sc.single = reinterpret_cast<const uint8_t*>(d_in);
+    sc.in_bytes = in_bytes;
+    sc.S = 1;
+    sc.n = n;
+    sc.offsets = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.offsets);
+    sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    sc.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
+    sc.n_flag_words = ranges_of(units);
+    sc.status = d_status;
     DecompressArgs a{};
     a.in = reinterpret_cast<const uint8_t*>(d_in);
     a.in_bytes = in_bytes;
     a.out = d_out;
     a.n = n;
-    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
-    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.offsets = sc.offsets;
     a.status = d_status;
-    const uint32_t grid = grid_for(units, dev->decompress_per_sm, dev->sms);
-    return launch_decompress(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+    return launch_decompress(sc, a, grid_for(ranges_of(units), dev->scan_per_sm, dev->sms),
+                             grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
 }
 
 zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
@@ -217,23 +284,34 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
         d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
         return ZCCL_ERR_INVALID_ARG;
     const uint64_t units = units_of(n);
-    if (ws_bytes < ws_bytes_for_units(units * S)) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const ScanLayout l = scan_layout(units, S);
+    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
 
+    ScanArgs sc{};
+    sc.streams = d_streams;
+    sc.in_bytes_dev = d_in_bytes;
+    sc.S = S;
+    sc.n = n;
+    sc.offsets = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.offsets);
+    sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    sc.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
+    sc.n_flag_words = (uint64_t)S * ranges_of(units);
+    sc.status = d_status;
     ReduceArgs a{};
     a.streams = d_streams;
     a.in_bytes = d_in_bytes;
     a.S = S;
     a.out = d_out;
     a.n = n;
-    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
-    a.n_flag_words = (ws_bytes - kCtrlBytes) / 8;
+    a.offsets = sc.offsets;
     a.status = d_status;
     const int per_sm = S <= kSmallShards ? dev->reduce_per_sm_small : dev->reduce_per_sm_large;
-    const uint32_t grid = grid_for(units, per_sm, dev->sms);
-    return launch_reduce(a, grid, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
+    return launch_reduce(sc, a, grid_for((uint64_t)S * ranges_of(units), dev->scan_per_sm, dev->sms),
+                         grid_for(units, per_sm, dev->sms), stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
 }
 
 const char* zccl_status_string(zccl_status_t s)

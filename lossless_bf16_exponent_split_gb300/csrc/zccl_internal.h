@@ -12,15 +12,34 @@ namespace zccl {
 
 struct WsCtrl;
 
+// Compression, one stream or a batch of segments (blocks + placement kernels).
 struct CompressArgs {
     const zccl_segment_t* segs;  // device descriptors (batched) or nullptr
     zccl_segment_t single;       // the one segment when segs == nullptr
     uint32_t n_segs;
-    uint32_t max_units;          // flag words available = chunk capacity
+    uint32_t max_units;          // chunks the workspace has room for
+    uint32_t max_ranges;         // scan ranges (look-back flags) it has room for
     uint8_t lut[8];
     uint64_t* out_bytes;         // device [n_segs]
     WsCtrl* ctrl;
-    uint64_t* flags;
+    uint64_t* flags;             // [max_ranges]
+    uint64_t n_flag_words;
+    uint32_t* counts;            // [max_units] escapes per chunk
+    uint8_t* stage;              // [max_units * 4096] escapes, chunk-local
+    uint32_t* status;
+};
+
+// Escape-offset scan over S streams of n elements (decompress: S = 1).
+struct ScanArgs {
+    const void* const* streams;  // device [S], or nullptr with `single`
+    const uint8_t* single;
+    const uint64_t* in_bytes_dev;  // device [S], or nullptr with `in_bytes`
+    uint64_t in_bytes;
+    uint32_t S;
+    uint64_t n;
+    uint64_t* offsets;           // [S][units + 1]
+    WsCtrl* ctrl;
+    uint64_t* flags;             // [S][ranges per stream]
     uint64_t n_flag_words;
     uint32_t* status;
 };
@@ -30,9 +49,7 @@ struct DecompressArgs {
     uint64_t in_bytes;
     uint16_t* out;
     uint64_t n;
-    WsCtrl* ctrl;
-    uint64_t* flags;
-    uint64_t n_flag_words;
+    const uint64_t* offsets;     // [units + 1], from the scan
     uint32_t* status;
 };
 
@@ -42,20 +59,44 @@ struct ReduceArgs {
     uint32_t S;
     uint16_t* out;
     uint64_t n;
-    WsCtrl* ctrl;
-    uint64_t* flags;             // [S][units]
-    uint64_t n_flag_words;
+    const uint64_t* offsets;     // [S][units + 1], from the scan
     uint32_t* status;
 };
 
-size_t compress_smem_bytes(uint32_t n_segs);
-cudaError_t launch_compress(const CompressArgs& a, uint32_t grid, cudaStream_t stream);
-int compress_ctas_per_sm(uint32_t n_segs);
+// Launches `kernel` on `stream` so that it may start while the previous
+// kernel on the stream finishes (programmatic dependent launch); the kernel
+// itself waits (griddepcontrol.wait) before reading the previous kernel's
+// results.
+template <typename Args>
+cudaError_t launch_dependent(void (*kernel)(Args), uint32_t grid, uint32_t threads, size_t smem,
+                             cudaStream_t stream, const Args& a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
-cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream);
+size_t compress_smem_bytes(uint32_t n_segs);
+cudaError_t launch_compress(const CompressArgs& a, uint32_t grid_blocks, uint32_t grid_place, cudaStream_t stream);
+int compress_ctas_per_sm(uint32_t n_segs);
+int place_ctas_per_sm(uint32_t n_segs);
+
+cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream);
+int scan_ctas_per_sm();
+cudaError_t launch_decompress(const ScanArgs& s, const DecompressArgs& a, uint32_t grid_scan, uint32_t grid,
+                              cudaStream_t stream);
 int decompress_ctas_per_sm();
 
-cudaError_t launch_reduce(const ReduceArgs& a, uint32_t grid, cudaStream_t stream);
+cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
+                          cudaStream_t stream);
 int reduce_ctas_per_sm(uint32_t S);
 
 }  // namespace zccl

@@ -10,17 +10,20 @@
 // add an IEEE fp32 add (no FMA, no flush to zero) in shard order, x_s decoded
 // from stream s; a NaN sum becomes 0x7FC0.
 //
-// GB300 design.  A CTA takes a 4096-element chunk by ticket and walks its S
-// shard blocks in order through a 3-stage ring of shared buffers filled by
-// TMA bulk copies (two steps in flight while one decodes).  For each shard
-// block it counts escapes from the planes, runs that shard's decoupled
-// look-back (one flag array per shard), gathers the shard's escapes and
-// decodes 32 elements per thread straight into fp32 accumulators held in
-// registers; after the last shard it rounds and stores 16-byte vectors.  The
-// compressed shards are read once and the BF16 result written once.
+// GB300 design: the escape scan kernel (zccl_decompress.cu) first computes
+// every shard's per-chunk zero-point offsets from the code planes; then,
+// started by programmatic dependent launch, reduce_kernel walks the chunks
+// (persistent grid, static stride) and, for each chunk, the S shard blocks
+// in order through a 3-stage ring of shared buffers: each step is one TMA
+// bulk copy of the shard's block plus one of its zero-point run, so two
+// steps are in flight while one decodes.  Each thread decodes 32 elements of
+// the step straight into fp32 accumulators held in registers; after the
+// last shard it rounds and stores 16-byte vectors.  Every compressed byte is
+// read once and the BF16 result written once.
 #include <cstdint>
 
 #include "zccl_common.cuh"
+#include "zccl_decode.cuh"
 #include "zccl_internal.h"
 
 namespace zccl {
@@ -32,56 +35,15 @@ constexpr int kStages = 3;
 
 struct __align__(16) ReduceSmem {
     uint8_t blk[kStages][kBlockBytes];
+    uint8_t zpb[kStages][kZpBufBytes];
     uint8_t expo[kChunk];
     uint64_t bar[kStages];
-    uint32_t stage_unit[kStages];
-    uint32_t stage_shard[kStages];
+    uint32_t zdelta[kStages];
+    uint32_t zcount[kStages];
     uint32_t scan[kThreads / 32];
-    uint32_t gen;
-    uint32_t flag;
-    uint32_t lb_status;
     uint32_t abort;
-    uint32_t load_unit;
-    uint32_t ended;
-    uint64_t lb_prefix;
 };
 // followed by per-shard tables: const uint8_t* base[S]; uint64_t n_esc[S]; uint32_t lut[S][2]
-
-__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
-
-__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x)
-{
-    x = (x | (x << 12)) & 0x000F000Fu;
-    x = (x | (x << 6)) & 0x03030303u;
-    x = (x | (x << 3)) & 0x11111111u;
-    return x;
-}
-
-__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
-                                         uint32_t lut_hi, uint2 xe)
-{
-    const uint32_t N = spread_nibbles(pb0) | (spread_nibbles(pb1) << 1) | (spread_nibbles(pb2) << 2);
-    uint32_t e_lo = __byte_perm(lut_lo, lut_hi, N);
-    uint32_t e_hi = __byte_perm(lut_lo, lut_hi, N >> 16);
-    const uint32_t m_lo = __byte_perm(0xFFu, 0u, N);
-    const uint32_t m_hi = __byte_perm(0xFFu, 0u, N >> 16);
-    e_lo = (e_lo & ~m_lo) | (xe.x & m_lo);
-    e_hi = (e_hi & ~m_hi) | (xe.y & m_hi);
-    const uint32_t lo_a = (smb.x & 0x7F7F7F7Fu) | ((e_lo << 7) & 0x80808080u);
-    const uint32_t hi_a = (smb.x & 0x80808080u) | ((e_lo >> 1) & 0x7F7F7F7Fu);
-    const uint32_t lo_b = (smb.y & 0x7F7F7F7Fu) | ((e_hi << 7) & 0x80808080u);
-    const uint32_t hi_b = (smb.y & 0x80808080u) | ((e_hi >> 1) & 0x7F7F7F7Fu);
-    return make_uint4(__byte_perm(lo_a, hi_a, 0x5140), __byte_perm(lo_a, hi_a, 0x7362),
-                      __byte_perm(lo_b, hi_b, 0x5140), __byte_perm(lo_b, hi_b, 0x7362));
-}
-
-// fp32 -> BF16, round to nearest, ties to even; NaN -> 0x7FC0.
-__device__ __forceinline__ uint32_t rne_bf16(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
-    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
-}
 
 struct ShardTables {
     const uint8_t** base;
@@ -99,27 +61,37 @@ __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t 
     return t;
 }
 
-// Thread 0: queue the load of step j (unit = j / S-th ticket, shard j % S).
-__device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t,
-                                           uint32_t j, uint32_t total_units)
+// Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / S) * gridDim.x,
+// shard j % S) into stage j % kStages.
+__device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t j,
+                                           uint32_t total)
 {
-    const int stage = j % kStages;
+    const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
+    if (c >= total) return;
     const uint32_t s = j % a.S;
-    if (s == 0 && !sm.ended) {
-        sm.load_unit = atomicAdd(&a.ctrl->ticket, 1u);
-        if (sm.load_unit >= total_units) sm.ended = 1;
-    }
-    if (sm.ended) {
-        sm.stage_unit[stage] = 0xFFFFFFFFu;
-        return;
-    }
-    const uint32_t unit = sm.load_unit;
-    sm.stage_unit[stage] = unit;
-    sm.stage_shard[stage] = s;
-    const uint32_t valid = (uint32_t)umin64(kChunk, a.n - (uint64_t)unit * kChunk);
+    const int st = j % kStages;
+    const uint32_t units = total;
+    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    mbar_arrive_expect_tx(&sm.bar[stage], bytes);
-    bulk_g2s(sm.blk[stage], t.base[s] + kHeaderBytes + (uint64_t)unit * kBlockBytes, bytes, &sm.bar[stage]);
+    const uint64_t* off = a.offsets + (uint64_t)s * (units + 1);
+    const uint64_t o0 = off[c], o1 = off[c + 1];
+    uint32_t zbytes = 0, delta = 0, cnt = 0;
+    const uint64_t zp = zp_offset_of(a.n);
+    if (o1 >= o0 && o1 <= t.n_esc[s] && o1 - o0 <= kChunk) {
+        cnt = (uint32_t)(o1 - o0);
+        if (cnt) {
+            const uint64_t lo = zp + o0, lo16 = lo & ~15ull, hi16 = round_up(zp + o1, 16);
+            zbytes = (uint32_t)(hi16 - lo16);
+            delta = (uint32_t)(lo - lo16);
+        }
+    } else {
+        report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+    }
+    sm.zdelta[st] = delta;
+    sm.zcount[st] = cnt;
+    mbar_arrive_expect_tx(&sm.bar[st], bytes + zbytes);
+    bulk_g2s(sm.blk[st], t.base[s] + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[st]);
+    if (zbytes) bulk_g2s(sm.zpb[st], t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
 }
 
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
@@ -128,9 +100,10 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
     ReduceSmem& sm = *reinterpret_cast<ReduceSmem*>(smem_raw);
     const ShardTables t = shard_tables(smem_raw, a.S);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t total_units = (uint32_t)units_of(a.n);
+    const uint32_t total = (uint32_t)units_of(a.n);
 
-    // ---- prologue: validate every shard's header, keep what decoding needs ----
+    // every shard's header (the scan kernel reports a bad one; here it only
+    // stops this kernel from reading out of bounds)
     bool ok = true;
     for (uint32_t s = tid; s < a.S; s += kThreads) {
         const uint8_t* base = reinterpret_cast<const uint8_t*>(a.streams[s]);
@@ -153,85 +126,55 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
         fence_mbar_init();
-        sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
         sm.abort = 0;
-        sm.ended = 0;
     }
-    const bool all_ok = __syncthreads_and(ok) != 0;
-    const uint32_t tag = tag_of_gen(sm.gen);
-    if (!all_ok) {
-        if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-        finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
-        return;
-    }
+    pdl_wait();  // offsets of the scan kernel
+    if (!__syncthreads_and(ok)) return;
 
     if (tid == 0)
-        for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total_units);
-    __syncthreads();
+        for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total);
 
     float acc[32];
 #pragma unroll
     for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
 
-    uint32_t k = 0;
-    for (;; ++k) {
-        const int stage = k % kStages;
-        if (tid == 0) issue_step(a, sm, t, k + kStages - 1, total_units);
-        const uint32_t unit = sm.stage_unit[stage];
-        if (unit >= total_units) break;
-        const uint32_t s = sm.stage_shard[stage];
-        const uint64_t first = (uint64_t)unit * kChunk;
-        const uint32_t valid = (uint32_t)umin64(kChunk, a.n - first);
+    uint32_t j = 0;
+    for (;; ++j) {
+        const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
+        if (c >= total) break;
+        const uint32_t s = j % a.S;
+        const int st = j % kStages;
+        if (tid == 0) issue_step(a, sm, t, j + kStages - 1, total);
+        const uint64_t first = (uint64_t)c * kChunk;
+        const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
-        if (!mbar_wait(&sm.bar[stage], (k / kStages) & 1)) atomicExch(&sm.abort, 1u);
+        if (!mbar_wait(&sm.bar[st], (j / kStages) & 1)) atomicExch(&sm.abort, 1u);
         __syncthreads();
         if (sm.abort) {
-            if (tid == 0) {
-                report(a.status, ZCCL_ERR_TIMEOUT);
-                st_release(&a.flags[(uint64_t)s * total_units + unit], make_flag(kFlagPoison, tag, 0));
-            }
+            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
             break;
         }
-        const uint8_t* blk = sm.blk[stage];
-
+        const uint8_t* blk = sm.blk[st];
         uint32_t esc = 0;
         if (tid < (int)(L / 32)) {
             const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-            const uint32_t p0 = pw[tid], p1 = pw[L / 32 + tid], p2 = pw[L / 16 + tid];
             const uint32_t w0 = 32u * tid;
             const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
                                    : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-            esc = ~(p0 | p1 | p2) & vmask;
+            esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
         }
         uint32_t agg;
         const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
-        if (warp == 0) {
-            uint64_t pre;
-            const uint32_t st = lookback(a.flags + (uint64_t)s * total_units, unit, 0, agg, tag, &pre);
-            if (lane == 0) {
-                sm.lb_status = st;
-                sm.lb_prefix = pre;
+        if (agg == sm.zcount[st]) {
+            const uint8_t* src = sm.zpb[st] + sm.zdelta[st] + excl;
+            uint32_t m = esc, jj = 0;
+            while (m) {
+                const uint32_t b = __ffs(m) - 1;
+                m &= m - 1;
+                sm.expo[32u * tid + b] = src[jj++];
             }
-        }
-        __syncthreads();
-        bool good = sm.lb_status == ZCCL_OK;
-        if (!good) {
-            if (tid == 0) report(a.status, sm.lb_status);
-        } else {
-            const uint64_t P = sm.lb_prefix;
-            const uint64_t n_esc = t.n_esc[s];
-            if (P + agg > n_esc || (unit + 1 == total_units && P + agg != n_esc)) {
-                if (tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-                good = false;
-            } else {
-                const uint8_t* src = t.base[s] + zp_offset_of(a.n) + P + excl;
-                uint32_t m = esc, j = 0;
-                while (m) {
-                    const uint32_t b = __ffs(m) - 1;
-                    m &= m - 1;
-                    sm.expo[32u * tid + b] = src[j++];
-                }
-            }
+        } else if (tid == 0) {
+            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
         }
         __syncthreads();
         const uint32_t lut_lo = t.lut[2 * s], lut_hi = t.lut[2 * s + 1];
@@ -239,12 +182,9 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
         for (int i = 0; i < 4; ++i) {
             const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
             if (e0 < L) {
-                const uint2 smb = *reinterpret_cast<const uint2*>(blk + e0);
-                const uint32_t pb0 = blk[L + (e0 >> 3)];
-                const uint32_t pb1 = blk[L + L / 8 + (e0 >> 3)];
-                const uint32_t pb2 = blk[L + L / 4 + (e0 >> 3)];
-                const uint2 xe = *reinterpret_cast<const uint2*>(sm.expo + e0);
-                const uint4 o = decode8(smb, pb0, pb1, pb2, lut_lo, lut_hi, xe);
+                const uint4 o = decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
+                                        blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
+                                        *reinterpret_cast<const uint2*>(sm.expo + e0));
                 const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -266,40 +206,41 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
             for (int i = 0; i < 4; ++i) {
                 const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
                 if (e0 >= valid) continue;
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    w[q] = rne_bf16(acc[8 * i + 2 * q]) | (rne_bf16(acc[8 * i + 2 * q + 1]) << 16);
+                uint4 o;
+                o.x = rne_bf16(acc[8 * i + 0]) | (rne_bf16(acc[8 * i + 1]) << 16);
+                o.y = rne_bf16(acc[8 * i + 2]) | (rne_bf16(acc[8 * i + 3]) << 16);
+                o.z = rne_bf16(acc[8 * i + 4]) | (rne_bf16(acc[8 * i + 5]) << 16);
+                o.w = rne_bf16(acc[8 * i + 6]) | (rne_bf16(acc[8 * i + 7]) << 16);
                 if (e0 + 8 <= valid) {
-                    *reinterpret_cast<uint4*>(dst + e0) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(dst + e0) = o;
                 } else {
-                    for (uint32_t q = 0; q < valid - e0; ++q)
-                        dst[e0 + q] = (uint16_t)(w[q >> 1] >> (16 * (q & 1)));
+                    store_partial(dst + e0, o, valid - e0);
                 }
             }
         }
         __syncthreads();
     }
-    // loads still in flight (steps issued but not consumed): wait, bounded
-    if (tid == 0) {
-        for (uint32_t j = k + 1; j < k + kStages; ++j) {
-            if (sm.stage_unit[j % kStages] < total_units) mbar_wait(&sm.bar[j % kStages], (j / kStages) & 1);
+    // steps still in flight after an early stop: wait for them (bounded)
+    if (tid == 0 && sm.abort) {
+        for (uint32_t jj = j + 1; jj < j + kStages; ++jj) {
+            if (blockIdx.x + (jj / a.S) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
         }
     }
-    finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
 }
 
 }  // namespace
 
 static size_t reduce_smem_bytes(uint32_t S) { return sizeof(ReduceSmem) + 24ull * S; }
 
-cudaError_t launch_reduce(const ReduceArgs& a, uint32_t grid, cudaStream_t stream)
+cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
+                          cudaStream_t stream)
 {
     const size_t smem = reduce_smem_bytes(a.S);
     cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    reduce_kernel<<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    e = launch_scan(s, grid_scan, stream);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(reduce_kernel, grid, kThreads, smem, stream, a);
 }
 
 int reduce_ctas_per_sm(uint32_t S)
