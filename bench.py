@@ -69,8 +69,12 @@ def source_sha(names):
     return h.hexdigest()[:16]
 
 
-KERNEL_SOURCES = {"compress_kernel": ["zccl_compress.cu"], "decompress_kernel": ["zccl_decompress.cu"],
-                  "reduce_kernel": ["zccl_reduce.cu"]}
+# each op = two launches of the kernels in these sources (plus zccl_common.cuh)
+KERNEL_SOURCES = {"compress": ["zccl_compress.cu"], "decompress": ["zccl_decompress.cu", "zccl_decode.cuh"],
+                  "decompress_reduce": ["zccl_reduce.cu", "zccl_decompress.cu", "zccl_decode.cuh"]}
+OP_KERNELS = {"compress": "compress_blocks_kernel + compress_place_kernel",
+              "decompress": "escape_scan_kernel + decompress_kernel",
+              "decompress_reduce": "escape_scan_kernel + reduce_kernel"}
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -333,9 +337,9 @@ def main():
             comp(r)
         torch.cuda.synchronize()
         stream_bytes = int(nbs[0].item())
-        launches_per_step = 2
-        names = ["compress_kernel", "decompress_kernel"]
-        alg = {"compress_kernel": 2 * n + stream_bytes, "decompress_kernel": stream_bytes + 2 * n}
+        launches_per_step = 4
+        names = ["compress", "decompress"]
+        alg = {"compress": 2 * n + stream_bytes, "decompress": stream_bytes + 2 * n}
         step_input_bytes = 2 * 2 * n
 
         def step(k, ev=None):
@@ -376,9 +380,9 @@ def main():
         comp()
         torch.cuda.synchronize()
         sb = int(nb.sum().item())
-        launches_per_step = 1
-        names = ["compress_kernel"]
-        alg = {"compress_kernel": 2 * total_n + sb}
+        launches_per_step = 2
+        names = ["compress"]
+        alg = {"compress": 2 * total_n + sb}
         step_input_bytes = 2 * total_n
 
         def step(k, ev=None):
@@ -413,9 +417,9 @@ def main():
         def red():
             z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n, ws.data_ptr(),
                                              wsb, st_ptr, h), "decompress_reduce")
-        launches_per_step = 1
-        names = ["reduce_kernel"]
-        alg = {"reduce_kernel": sum(sizes_h) + 2 * n}
+        launches_per_step = 2
+        names = ["decompress_reduce"]
+        alg = {"decompress_reduce": sum(sizes_h) + 2 * n}
         step_input_bytes = 2 * S * n
 
         def step(k, ev=None):
@@ -510,7 +514,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
         "config": {"workload": args.workload, "desc": workload_desc(args.workload), **cfg_extra,
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 2), "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "launches": OP_KERNELS[dom],
+                     "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(dom, args.workload),
                      "algorithmic_bytes_per_launch": alg[dom]},

@@ -42,12 +42,14 @@
  *     before the call and read it after the stream has synchronised;
  *   - n is limited to 2^40 elements per stream.
  *
- * Workspace: a device buffer of zccl_workspace_bytes() bytes that the
- * kernels use to order their chunks (a ticket counter and one flag word per
- * chunk for the single-pass scan of escape counts).  It must be zeroed once
- * before its first use (zccl_workspace_init or any memset to 0); every call
- * leaves it ready for the next one.  A workspace must not be used by two
- * calls that may run at the same time (different streams): they would race.
+ * Workspace: a device buffer of zccl_workspace_bytes() bytes that holds a
+ * call's intermediate results: per-chunk escape counts and the per-range
+ * totals and bases of the device-wide scan (compression also stages each
+ * chunk's escapes there, up to 4096 bytes per chunk, so its workspace is
+ * about n bytes).  It must be zeroed once before its first use
+ * (zccl_workspace_init or any memset to 0); every call leaves it ready for
+ * the next one.  A workspace must not be used by two calls that may run at
+ * the same time (different streams): they would race.
  */
 #ifndef ZCCL_H
 #define ZCCL_H
@@ -167,6 +169,14 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
                                      uint32_t S, uint16_t* d_out, uint64_t n, void* d_ws,
                                      uint64_t ws_bytes, uint32_t* d_status,
                                      cudaStream_t stream);
+
+/* Diagnostic of the bounded device waits.  The kernels' only waits are on
+ * barriers completed by their own TMA copies; each gives up after a limit
+ * and reports ZCCL_ERR_TIMEOUT rather than hang.  This call runs that same
+ * wait, with a limit of limit_us microseconds (1..1,000,000), on a barrier
+ * that nothing completes, so *d_status must become ZCCL_ERR_TIMEOUT.  The
+ * paper has no counterpart; it exists to test the failure path. */
+zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream);
 
 /* Static text for a status code. */
 const char* zccl_status_string(zccl_status_t status);

@@ -51,6 +51,7 @@ _SIGS = {
     "zccl_decompress_reduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
                                 ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                 ctypes.c_void_p], ctypes.c_int),
+    "zccl_check_bounded_wait": ([ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_status_string": ([ctypes.c_int], ctypes.c_char_p),
 }
 
@@ -134,6 +135,10 @@ def zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes, d
                            stream) -> int:
     return lib().zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes,
                                         d_status, stream)
+
+
+def zccl_check_bounded_wait(limit_us, d_status, stream) -> int:
+    return lib().zccl_check_bounded_wait(limit_us, d_status, stream)
 
 
 def zccl_status_string(status: int) -> str:

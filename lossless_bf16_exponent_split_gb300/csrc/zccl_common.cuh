@@ -49,27 +49,18 @@ __host__ __device__ inline uint64_t stream_bytes_of(uint64_t n, uint64_t n_esc)
 }
 
 // ---- workspace --------------------------------------------------------------
-// [0,128): control words; then one 64-bit look-back flag per chunk (per shard
-// and chunk for the reduction).
+// [0,128): control words (the rest of the workspace is laid out per call by
+// the host layer).
 struct WsCtrl {
-    uint32_t ticket;  // next chunk ticket of the running call; 0 between calls
-    uint32_t done;    // CTAs finished (wraps to 0 at gridDim.x via atomicInc)
-    uint32_t gen;     // calls completed on this workspace; tags the flags
-    uint32_t pad[29];
+    uint32_t done;  // CTAs finished in the running call; wraps to 0 at gridDim.x
+    uint32_t pad[31];
 };
 static_assert(sizeof(WsCtrl) == 128, "control block is 128 bytes");
 constexpr uint64_t kCtrlBytes = 128;
 
-// flag word: [63:62] state, [61:40] call tag, [39:0] value
-constexpr uint64_t kFlagAgg = 1, kFlagPrefix = 2, kFlagPoison = 3;
-constexpr uint32_t kTagMod = (1u << 22) - 1;  // tags run 1..kTagMod
-constexpr uint64_t kValueMask = (1ull << 40) - 1;
-
-__device__ __forceinline__ uint32_t tag_of_gen(uint32_t gen) { return gen % kTagMod + 1; }
-__device__ __forceinline__ uint64_t make_flag(uint64_t state, uint32_t tag, uint64_t v)
-{
-    return (state << 62) | ((uint64_t)tag << 40) | (v & kValueMask);
-}
+// Chunks per range: the unit of the per-range escape totals that one CTA
+// scans at the end of a pass.
+constexpr uint32_t kRangeChunks = 32;
 
 // A bounded wait gives up after this long (then reports ZCCL_ERR_TIMEOUT).
 constexpr uint64_t kSpinTimeoutNs = 1000000000ull;
@@ -142,14 +133,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Bounded wait for phase `parity` of `bar`; false if it did not complete
-// within kSpinTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+// within `limit_ns` (the copies it waits for are then reported lost).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kSpinTimeoutNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15) == 0 && globaltimer() - t0 > kSpinTimeoutNs) return false;
+        if ((it & 15) == 0 && globaltimer() - t0 > limit_ns) return false;
     }
 }
 
@@ -220,86 +211,6 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* scratch, T* total)
     return before + incl - v;
 }
 
-// ---- decoupled look-back ----------------------------------------------------
-// Called by one full warp for work unit `unit` whose scan segment starts at
-// `seg_first`.  Publishes `agg` (the unit's escape count), reads predecessors'
-// flags 32*kPerLane at a time (each lane kPerLane of them, bounded waits) and
-// returns the exclusive prefix in *exclusive.  Units are taken by ticket, so
-// every predecessor is held by a CTA that is running or done and every wait
-// ends; a wait that still runs out (or a poisoned predecessor) marks this
-// unit poisoned and returns ZCCL_ERR_TIMEOUT.
-template <int kPerLane>
-__device__ inline uint32_t lookback(uint64_t* flags, uint32_t unit, uint32_t seg_first, uint64_t agg,
-                                    uint32_t tag, uint64_t* exclusive)
-{
-    const int lane = threadIdx.x & 31;
-    if (unit == seg_first) {
-        if (lane == 0) st_release(&flags[unit], make_flag(kFlagPrefix, tag, agg));
-        *exclusive = 0;
-        return ZCCL_OK;
-    }
-    if (lane == 0) st_release(&flags[unit], make_flag(kFlagAgg, tag, agg));
-    uint64_t excl = 0;
-    int64_t base = (int64_t)unit - 1;
-    const uint64_t t0 = globaltimer();
-    for (;;) {
-        uint64_t state[kPerLane], val[kPerLane];
-        bool timed_out = false;
-#pragma unroll
-        for (int q = 0; q < kPerLane; ++q) {
-            const int64_t idx = base - lane - 32 * q;  // distance lane + 32 q
-            state[q] = kFlagPrefix;
-            val[q] = 0;
-            if (idx >= (int64_t)seg_first && !timed_out) {
-                for (uint32_t it = 0;; ++it) {
-                    const uint64_t f = ld_acquire(&flags[idx]);
-                    if ((uint32_t)((f >> 40) & 0x3FFFFF) == tag && (f >> 62) != 0) {
-                        state[q] = f >> 62;
-                        val[q] = f & kValueMask;
-                        break;
-                    }
-                    if ((it & 31) == 31) {
-                        if (globaltimer() - t0 > kSpinTimeoutNs) {
-                            timed_out = true;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                }
-            }
-        }
-        bool bad_lane = timed_out;
-#pragma unroll
-        for (int q = 0; q < kPerLane; ++q) bad_lane = bad_lane || state[q] == kFlagPoison;
-        if (__ballot_sync(0xffffffffu, bad_lane)) {
-            if (lane == 0) st_release(&flags[unit], make_flag(kFlagPoison, tag, 0));
-            *exclusive = 0;
-            return ZCCL_ERR_TIMEOUT;
-        }
-        // nearest PREFIX: smallest distance lane + 32 q
-        bool found = false;
-        uint64_t part = 0;
-#pragma unroll
-        for (int q = 0; q < kPerLane; ++q) {
-            if (found) break;
-            const uint32_t pm = __ballot_sync(0xffffffffu, state[q] == kFlagPrefix);
-            if (pm) {
-                const int first = __ffs(pm) - 1;
-                part += lane <= first ? val[q] : 0;
-                found = true;
-            } else {
-                part += val[q];
-            }
-        }
-        excl += warp_sum_u64(part);
-        if (found) break;
-        base -= 32 * kPerLane;
-    }
-    if (lane == 0) st_release(&flags[unit], make_flag(kFlagPrefix, tag, excl + agg));
-    *exclusive = excl;
-    return ZCCL_OK;
-}
-
 // ---- programmatic dependent launch -------------------------------------------
 // The first kernel of a pair lets the second launch once its CTAs are done
 // with their main work; the second waits for the first's completion (and its
@@ -310,16 +221,12 @@ __device__ __forceinline__ void pdl_launch_dependents()
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Chunks per scan range of the small look-back kernels.
-constexpr uint32_t kRangeChunks = 32;
-
-// ---- end of a call ----------------------------------------------------------
-// Every CTA calls this once, last, with all its threads.  The CTA that
-// finishes last resets the ticket, advances the generation (so the next
-// call's flags carry a new tag) and, once every kTagMod calls, clears the
-// flags so a tag can never meet a stale flag of its own value.
-__device__ inline void finish_call(WsCtrl* ctrl, uint64_t* flags, uint64_t n_flag_words, uint32_t gen,
-                                   uint32_t* s_flag)
+// ---- last CTA of a grid --------------------------------------------------------
+// Every CTA calls this exactly once, with all its threads, after its last
+// global write of the pass.  It returns true in the one CTA that arrives
+// last, which may then read everything the others wrote; the counter wraps
+// back to 0 for the next call on the workspace.
+__device__ inline bool arrive_last(WsCtrl* ctrl, uint32_t* s_flag)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -328,18 +235,88 @@ __device__ inline void finish_call(WsCtrl* ctrl, uint64_t* flags, uint64_t n_fla
         *s_flag = (old == gridDim.x - 1) ? 1u : 0u;
     }
     __syncthreads();
-    if (*s_flag) {
-        const uint32_t next = gen + 1;
-        if (next % kTagMod == 0) {
-            for (uint64_t i = threadIdx.x; i < n_flag_words; i += blockDim.x) flags[i] = 0;
-            __threadfence();
-            __syncthreads();
+    const bool last = *s_flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// ---- segmented exclusive scan by one CTA --------------------------------------
+// out[r] = sum of in[q] for q in [head(r), r), where head(r) is the first
+// index of r's segment (is_head(q) marks segment starts).  One CTA of
+// kThreads threads, K values per thread per tile; loads bypass L1 (the
+// inputs were written by other CTAs).  Contains barriers.
+template <int kThreads, int K, class IsHead>
+__device__ void cta_segmented_exclusive_scan(const uint32_t* in, uint64_t* out, uint32_t R, IsHead is_head,
+                                             uint64_t* sv /*[kThreads/32]*/, uint32_t* sf /*[kThreads/32]*/)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t carry_v = 0;  // state after the previous tile
+    for (uint32_t base = 0; base < R; base += kThreads * K) {
+        const uint32_t first = base + threadIdx.x * K;
+        uint64_t v[K], loc[K];
+        bool h[K];
+        uint64_t acc = 0;
+        bool any = false;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const uint32_t r = first + j;
+            v[j] = r < R ? (uint64_t)__ldcg(in + r) : 0;
+            h[j] = r < R && is_head(r);
         }
-        if (threadIdx.x == 0) {
-            atomicExch(&ctrl->ticket, 0u);
-            __threadfence();
-            atomicExch(&ctrl->gen, next);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (h[j]) {
+                acc = 0;
+                any = true;
+            }
+            acc += v[j];
+            loc[j] = acc;
         }
+        // (f, x): f = a segment starts inside, x = sum since the last start
+        uint32_t f = any;
+        uint64_t x = acc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t fu = __shfl_up_sync(0xffffffffu, f, o);
+            const uint64_t xu = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) {
+                if (!f) x += xu;
+                f |= fu;
+            }
+        }
+        if (lane == 31) {
+            sf[warp] = f;
+            sv[warp] = x;
+        }
+        // exclusive state within the warp
+        uint32_t fe = __shfl_up_sync(0xffffffffu, f, 1);
+        uint64_t xe = __shfl_up_sync(0xffffffffu, x, 1);
+        if (lane == 0) {
+            fe = 0;
+            xe = 0;
+        }
+        __syncthreads();
+        // prefix: carry, then earlier warps, then earlier lanes
+        uint32_t pf = 0;
+        uint64_t px = carry_v;
+        for (int w = 0; w < warp; ++w) {
+            px = sf[w] ? sv[w] : px + sv[w];
+            pf |= sf[w];
+        }
+        px = fe ? xe : px + xe;
+        bool seen = false;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            seen = seen || h[j];
+            const uint32_t r = first + j;
+            if (r < R) out[r] = (seen ? 0 : px) + loc[j] - v[j];
+        }
+        // state after the whole tile, for the next one
+        uint64_t tx = carry_v;
+        for (int w = 0; w < kThreads / 32; ++w) tx = sf[w] ? sv[w] : tx + sv[w];
+        __syncthreads();
+        carry_v = tx;
+        (void)pf;
     }
 }
 

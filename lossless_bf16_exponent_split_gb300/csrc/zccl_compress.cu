@@ -23,12 +23,14 @@
 //    pre-spread one byte apart, accumulated into one word whose bytes are the
 //    three plane bytes.  The coded block leaves by one bulk store.  popc over
 //    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
-//    chunk into a staging slot of the workspace and the count is recorded.
-//    No CTA ever waits for another.
-//  compress_place_kernel  scans the per-chunk counts in ranges of 32 chunks
-//    (ticket-ordered decoupled look-back, 128 flags read per round, bounded
-//    waits), copies each chunk's staged escapes to its place in the
-//    zero-point array, and finishes each stream (header, padding, size).
+//    chunk into a staging slot of the workspace, the count is recorded and
+//    added (one atomic) to its 32-chunk range's total.  No CTA waits for
+//    another: the CTA that finishes last (an atomic arrival counter) runs one
+//    segmented exclusive scan over the few hundred range totals -- the
+//    device-wide scan of the escape counts -- giving each range's base.
+//  compress_place_kernel  one CTA per range: scans its 32 counts, copies
+//    each chunk's staged escapes to base + prefix in the zero-point array,
+//    and finishes each stream (header, padding, size).
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -113,7 +115,9 @@ struct __align__(16) BlocksSmem {
     uint64_t bar[2];
     uint64_t scan64[kThreads / 32];
     uint32_t scan[kThreads / 32];
+    uint32_t scan_f[kThreads / 32];
     uint32_t abort;
+    uint32_t last;
 };
 
 __device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, BlocksSmem& sm,
@@ -149,11 +153,8 @@ __global__ void __launch_bounds__(kThreads) compress_blocks_kernel(const Compres
     }
     uint64_t total64, ranges64;
     segment_table(a, ustart, rstart, sm.scan64, &total64, &ranges64);
-    if (total64 > a.max_units) {  // reported by the placement kernel
-        pdl_launch_dependents();
-        return;
-    }
-    const uint32_t total = (uint32_t)total64;
+    const bool fits = total64 <= a.max_units && ranges64 <= a.max_ranges;  // else reported by the placement kernel
+    const uint32_t total = fits ? (uint32_t)total64 : 0u;
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
@@ -253,12 +254,22 @@ __global__ void __launch_bounds__(kThreads) compress_blocks_kernel(const Compres
         }
         if (tid == 0) {
             a.counts[c] = agg;
+            if (agg) atomicAdd(&a.totals[rstart[s] + cl / kRangeChunks], agg);
             bulk_wait_read0();
         }
         __syncthreads();
     }
     if (tid == 0) bulk_wait0();
     pdl_launch_dependents();
+    // the last CTA: exclusive scan of the range totals within each segment
+    if (arrive_last(a.ctrl, &sm.last) && fits) {
+        const uint32_t R = (uint32_t)ranges64;
+        cta_segmented_exclusive_scan<kThreads, 2>(
+            a.totals, a.bases, R,
+            [&](uint32_t r) { return rstart[find_segment(rstart, a.n_segs, r)] == r; }, sm.scan64, sm.scan_f);
+        // leave the totals at zero for the next call
+        for (uint32_t r = tid; r < R; r += kThreads) a.totals[r] = 0;
+    }
 }
 
 // ============================================================================
@@ -269,11 +280,6 @@ struct __align__(16) PlaceSmem {
     uint32_t scan[kThreads / 32];
     uint32_t cnt[kRangeChunks];
     uint32_t excl[kRangeChunks];
-    uint32_t ticket;
-    uint32_t gen;
-    uint32_t flag;
-    uint32_t lb_status;
-    uint64_t lb_prefix;
 };
 
 // Header of a finished stream (the 32 lanes of one warp write 4 bytes each).
@@ -306,12 +312,9 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
     uint32_t* rstart = ustart + a.n_segs + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    pdl_wait();  // counts and staged escapes of the blocks kernel
+    pdl_wait();  // counts, range bases and staged escapes of the blocks kernel
     uint64_t total_units, total_ranges;
     segment_table(a, ustart, rstart, sm.scan64, &total_units, &total_ranges);
-    if (tid == 0) sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
-    __syncthreads();
-    const uint32_t tag = tag_of_gen(sm.gen);
     if (blockIdx.x == 0 && a.segs != nullptr) {
         for (uint32_t s = tid; s < a.n_segs; s += kThreads) {
             const uint32_t bad = segment_error(a.segs[s]);
@@ -323,7 +326,6 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
     }
     if (total_units > a.max_units || total_ranges > a.max_ranges) {
         if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
-        finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
         return;
     }
     // empty, valid segments: header only (CTA 0)
@@ -337,11 +339,7 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
     }
 
     const uint32_t nr = (uint32_t)total_ranges;
-    for (;;) {
-        if (tid == 0) sm.ticket = atomicAdd(&a.ctrl->ticket, 1u);
-        __syncthreads();
-        const uint32_t r = sm.ticket;
-        if (r >= nr) break;
+    for (uint32_t r = blockIdx.x; r < nr; r += gridDim.x) {
         const uint32_t s = find_segment(rstart, a.n_segs, r);
         const zccl_segment_t d = seg_get(a, s);
         const uint32_t q = r - rstart[s];
@@ -349,44 +347,54 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
         const uint32_t c0 = q * kRangeChunks;                       // first chunk, segment-local
         const uint32_t nch = min(kRangeChunks, seg_units - c0);
         const uint32_t g0 = ustart[s] + c0;                          // first chunk, global
-        const uint32_t cnt = tid < (int)nch ? a.counts[g0 + tid] : 0u;
+        const uint32_t cnt = tid < (int)nch ? __ldcg(a.counts + g0 + tid) : 0u;
         uint32_t agg;
         const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
         if (tid < (int)kRangeChunks) {
             sm.cnt[tid] = cnt;
             sm.excl[tid] = ex;
         }
-        if (warp == 0) {
-            uint64_t pre;
-            const uint32_t st = lookback<4>(a.flags, r, rstart[s], agg, tag, &pre);
-            if (lane == 0) {
-                sm.lb_status = st;
-                sm.lb_prefix = pre;
+        __syncthreads();
+        const uint64_t P = __ldcg(a.bases + r);
+        const uint64_t zp = zp_offset_of(d.n);
+        uint8_t* out = (uint8_t*)d.out;
+        // each warp moves 8 chunks' staged escapes: all word loads first
+        // (one memory latency), then byte stores to the unaligned target
+        constexpr int kPerWarp = kRangeChunks / (kThreads / 32);
+        const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(a.stage);
+        uint32_t v[kPerWarp];
+#pragma unroll
+        for (int ii = 0; ii < kPerWarp; ++ii) {
+            const uint32_t i = warp + 4 * ii;
+            v[ii] = (i < nch && 4 * lane < sm.cnt[i]) ? __ldcg(stage32 + (uint64_t)(g0 + i) * (kChunk / 4) + lane)
+                                                       : 0u;
+        }
+#pragma unroll
+        for (int ii = 0; ii < kPerWarp; ++ii) {
+            const uint32_t i = warp + 4 * ii;
+            if (i >= nch) continue;
+            const uint32_t cnt_i = sm.cnt[i];
+            uint8_t* to = out + zp + P + sm.excl[i];
+#pragma unroll
+            for (uint32_t b = 0; b < 4; ++b)
+                if (4 * lane + b < cnt_i) to[4 * lane + b] = (uint8_t)(v[ii] >> (8 * b));
+            // escape-heavy chunks: the rest, 128 bytes per round
+            for (uint32_t w = 32 + lane; 4 * w < cnt_i; w += 32) {
+                const uint32_t x = __ldcg(stage32 + (uint64_t)(g0 + i) * (kChunk / 4) + w);
+#pragma unroll
+                for (uint32_t b = 0; b < 4; ++b)
+                    if (4 * w + b < cnt_i) to[4 * w + b] = (uint8_t)(x >> (8 * b));
             }
         }
-        __syncthreads();
-        if (sm.lb_status != ZCCL_OK) {
-            if (tid == 0) report(a.status, sm.lb_status);
-        } else {
-            const uint64_t P = sm.lb_prefix;
-            const uint64_t zp = zp_offset_of(d.n);
-            uint8_t* out = (uint8_t*)d.out;
-            for (uint32_t i = warp; i < nch; i += kThreads / 32) {
-                const uint8_t* from = a.stage + (uint64_t)(g0 + i) * kChunk;
-                uint8_t* to = out + zp + P + sm.excl[i];
-                for (uint32_t j = lane; j < sm.cnt[i]; j += 32) to[j] = from[j];
-            }
-            if (c0 + nch == seg_units) {  // last range: header, zero padding, size
-                const uint64_t n_esc = P + agg;
-                const uint64_t pad_end = round_up(n_esc, 128);
-                for (uint64_t b = n_esc + tid; b < pad_end; b += kThreads) out[zp + b] = 0;
-                if (warp == 1) write_header(out, d.n, n_esc, a.lut, lane);
-                if (tid == 0) a.out_bytes[s] = zp + pad_end;
-            }
+        if (c0 + nch == seg_units) {  // last range: header, zero padding, size
+            const uint64_t n_esc = P + agg;
+            const uint64_t pad_end = round_up(n_esc, 128);
+            for (uint64_t b = n_esc + tid; b < pad_end; b += kThreads) out[zp + b] = 0;
+            if (warp == 1) write_header(out, d.n, n_esc, a.lut, lane);
+            if (tid == 0) a.out_bytes[s] = zp + pad_end;
         }
         __syncthreads();
     }
-    finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
 }
 
 template <typename K>

@@ -11,15 +11,17 @@
 // launch.
 //
 //  escape_scan_kernel  reads only the code planes (3/8 byte per element).
-//    Each warp counts the escapes of a chunk with 16-byte loads and popc of
-//    ~(p0|p1|p2); ranges of 32 chunks are scanned across the grid by a
-//    ticket-ordered decoupled look-back (128 flags per round, bounded
-//    waits); the result is every chunk's offset into the zero-point array,
-//    plus the total, checked against the header.  It serves S streams at
-//    once for the fused reduction.
+//    One CTA per range of 32 chunks: each warp counts the escapes of 8 chunks
+//    with 16-byte loads (all issued first) and popc of ~(p0|p1|p2), and the
+//    CTA records each chunk's count and prefix within the range plus the
+//    range total.  No CTA waits for another: the CTA that finishes last (an
+//    atomic arrival counter) runs one segmented exclusive scan over the range
+//    totals -- the inverse of the encoder's device-wide scan -- and checks
+//    each stream's total against its header.  It serves S streams at once
+//    for the fused reduction.
 //  decompress_kernel  streams the blocks once: per chunk, one TMA bulk copy
 //    brings the block and a second brings the chunk's run of the zero-point
-//    array (known from the offsets), both completing on one mbarrier,
+//    array (at range base + prefix), both completing on one mbarrier,
 //    double-buffered.  Escaped exponents are scattered to their element slots
 //    in shared memory; each thread rebuilds 8 consecutive elements: plane
 //    bytes spread to nibble codes, one byte permute per 4 elements looks the
@@ -42,16 +44,28 @@ constexpr int kThreads = 128;
 // Kernel 1: escape offsets from the code planes
 // ============================================================================
 struct __align__(16) ScanSmem {
+    uint64_t scan64[kThreads / 32];
     uint32_t scan[kThreads / 32];
+    uint32_t scan_f[kThreads / 32];
     uint32_t cnt[kRangeChunks];
-    uint32_t ticket;
-    uint32_t gen;
-    uint32_t flag;
-    uint32_t lb_status;
     uint32_t hdr_ok;
-    uint64_t n_esc;
-    uint64_t lb_prefix;
+    uint32_t last;
 };
+
+// Header checks shared by the scan: magic, version, chunk size, n,
+// zp_offset, and that the zero-point array fits in in_bytes.
+__device__ __forceinline__ bool stream_header_ok(const uint8_t* base, uint64_t in_bytes, uint64_t n,
+                                                 uint64_t* n_esc_out)
+{
+    if (base == nullptr || ((uintptr_t)base & 15) != 0 || in_bytes < zp_offset_of(n)) return false;
+    const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
+    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+    const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
+    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+    *n_esc_out = n_esc;
+    return h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == n && zp == zp_offset_of(n) &&
+           n_esc <= n && zp + round_up(n_esc, 128) <= in_bytes;
+}
 
 __device__ __forceinline__ const uint8_t* scan_stream(const ScanArgs& a, uint32_t s)
 {
@@ -95,45 +109,47 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
     const uint32_t units = (uint32_t)units_of(a.n);
     const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;  // ranges per stream
     const uint32_t nr = rps * a.S;
-    if (tid == 0) sm.gen = *(volatile uint32_t*)&a.ctrl->gen;
-    __syncthreads();
-    const uint32_t tag = tag_of_gen(sm.gen);
 
-    for (;;) {
+    for (uint32_t r = blockIdx.x; r < nr; r += gridDim.x) {
+        const uint32_t s = r / rps, q = r % rps;
         if (tid == 0) {
-            const uint32_t r = atomicAdd(&a.ctrl->ticket, 1u);
-            sm.ticket = r;
-            if (r < nr) {  // header of this range's stream
-                const uint32_t s = r / rps;
-                const uint8_t* base = scan_stream(a, s);
-                const uint64_t in_bytes = scan_in_bytes(a, s);
-                bool ok = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
-                uint64_t n_esc = 0;
-                if (ok) {
-                    const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
-                    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-                    n_esc = h[4] | ((uint64_t)h[5] << 32);
-                    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-                    ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
-                         zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
-                }
-                sm.hdr_ok = ok;
-                sm.n_esc = n_esc;
-            }
+            uint64_t n_esc;
+            sm.hdr_ok = stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc);
         }
         __syncthreads();
-        const uint32_t r = sm.ticket;
-        if (r >= nr) break;
-        const uint32_t s = r / rps, q = r % rps;
         const uint32_t c0 = q * kRangeChunks;
         const uint32_t nch = min(kRangeChunks, units - c0);
         const bool ok = sm.hdr_ok != 0;
         if (ok) {
+            // each warp counts 8 chunks; the planes of all full chunks are
+            // loaded first (24 16-byte loads in flight per lane)
+            constexpr int kPerWarp = kRangeChunks / (kThreads / 32);
             const uint8_t* base = scan_stream(a, s);
-            for (uint32_t i = warp; i < nch; i += kThreads / 32) {
-                const uint32_t c = c0 + i;
-                const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
-                const uint32_t e = warp_chunk_escapes(base + kHeaderBytes + (uint64_t)c * kBlockBytes, valid);
+            uint4 p[kPerWarp][3];
+#pragma unroll
+            for (int ii = 0; ii < kPerWarp; ++ii) {
+                const uint32_t i = warp + 4 * ii;
+                const uint64_t c = c0 + i;
+                if (i < nch && (c + 1) * kChunk <= a.n) {
+                    const uint4* pw = reinterpret_cast<const uint4*>(base + kHeaderBytes + c * kBlockBytes + kChunk);
+#pragma unroll
+                    for (int qq = 0; qq < 3; ++qq) p[ii][qq] = __ldg(pw + qq * 32 + lane);
+                }
+            }
+#pragma unroll
+            for (int ii = 0; ii < kPerWarp; ++ii) {
+                const uint32_t i = warp + 4 * ii;
+                const uint64_t c = c0 + i;
+                if (i >= nch) continue;
+                uint32_t e;
+                if ((c + 1) * kChunk <= a.n) {
+                    e = __popc(~(p[ii][0].x | p[ii][1].x | p[ii][2].x)) + __popc(~(p[ii][0].y | p[ii][1].y | p[ii][2].y)) +
+                        __popc(~(p[ii][0].z | p[ii][1].z | p[ii][2].z)) + __popc(~(p[ii][0].w | p[ii][1].w | p[ii][2].w));
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+                } else {  // the stream's tail chunk
+                    e = warp_chunk_escapes(base + kHeaderBytes + c * kBlockBytes, (uint32_t)(a.n - c * kChunk));
+                }
                 if (lane == 0) sm.cnt[i] = e;
             }
         }
@@ -141,32 +157,34 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
         const uint32_t cnt = (ok && tid < (int)nch) ? sm.cnt[tid] : 0u;
         uint32_t agg;
         const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
-        if (warp == 0) {
-            uint64_t pre;
-            const uint32_t st = lookback<4>(a.flags, r, s * rps, agg, tag, &pre);
-            if (lane == 0) {
-                sm.lb_status = st;
-                sm.lb_prefix = pre;
-            }
+        if (tid < (int)nch) {
+            a.local[(uint64_t)s * units + c0 + tid] = ex;
+            a.count[(uint64_t)s * units + c0 + tid] = cnt;
         }
-        __syncthreads();
-        if (!ok) {
-            if (tid == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-        } else if (sm.lb_status != ZCCL_OK) {
-            if (tid == 0) report(a.status, sm.lb_status);
-        } else {
-            uint64_t* off = a.offsets + (uint64_t)s * (units + 1);
-            const uint64_t P = sm.lb_prefix;
-            if (tid < (int)nch) off[c0 + tid] = P + ex;
-            if (c0 + nch == units && tid == 0) {
-                off[units] = P + agg;
-                if (P + agg != sm.n_esc) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            }
-        }
+        if (tid == 0) a.totals[r] = agg;
         __syncthreads();
     }
     pdl_launch_dependents();
-    finish_call(a.ctrl, a.flags, a.n_flag_words, sm.gen, &sm.flag);
+    if (arrive_last(a.ctrl, &sm.last)) {
+        cta_segmented_exclusive_scan<kThreads, 8>(
+            a.totals, a.bases, nr, [&](uint32_t r) { return r % rps == 0; }, sm.scan64, sm.scan_f);
+        __syncthreads();
+        // every stream's recount must equal its header's escape count
+        for (uint32_t s = tid; s < a.S; s += kThreads) {
+            uint64_t n_esc = 0;
+            if (!stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc)) {
+                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            } else if (rps > 0) {
+                const uint32_t last = s * rps + rps - 1;
+                if (a.bases[last] + __ldcg(a.totals + last) != n_esc) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            } else if (n_esc != 0) {
+                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            }
+        }
+        __syncthreads();
+        // leave the totals at zero: every call on a workspace expects them so
+        for (uint32_t r = tid; r < nr; r += kThreads) a.totals[r] = 0;
+    }
 }
 
 // ============================================================================
@@ -190,9 +208,10 @@ __device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, Decod
 {
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint64_t o0 = a.offsets[c], o1 = a.offsets[c + 1];
+    const uint64_t o0 = __ldcg(a.bases + c / kRangeChunks) + __ldcg(a.local + c);
+    const uint64_t o1 = o0 + __ldcg(a.count + c);
     uint32_t zbytes = 0, delta = 0, cnt = 0;
-    if (o1 >= o0 && o1 <= sm.n_esc && o1 - o0 <= kChunk) {  // offsets checked by the scan kernel too
+    if (o1 <= sm.n_esc && o1 - o0 <= kChunk) {  // checked against the header by the scan kernel too
         cnt = (uint32_t)(o1 - o0);
         if (cnt) {
             const uint64_t lo = zp_offset_of(a.n) + o0, hi = zp_offset_of(a.n) + o1;
@@ -233,7 +252,7 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
         fence_mbar_init();
         sm.abort = 0;
     }
-    pdl_wait();  // offsets of the scan kernel
+    pdl_wait();  // counts, prefixes and range bases of the scan kernel
     __syncthreads();
     if (!sm.hdr_ok) return;  // reported by the scan kernel
     const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;

@@ -72,32 +72,37 @@ bool lut_ok(const zccl_lut_t* lut)
 
 uint64_t ranges_of(uint64_t units) { return (units + kRangeChunks - 1) / kRangeChunks; }
 
-// Compression workspace: control | look-back flag per range | escape count
-// per chunk | a 4096-byte escape staging slot per chunk.
+// Compression workspace: control | escape total per 32-chunk range (zero
+// between calls) | range base | escape count per chunk | a 4096-byte escape
+// staging slot per chunk.
 struct CompressLayout {
-    uint64_t flags, counts, stage, total;
+    uint64_t totals, bases, counts, stage, total;
 };
 CompressLayout compress_layout(uint64_t units, uint64_t ranges)
 {
     CompressLayout l;
-    l.flags = kCtrlBytes;
-    l.counts = l.flags + 8 * ranges;
+    l.totals = kCtrlBytes;
+    l.bases = round_up(l.totals + 4 * ranges, 16);
+    l.counts = round_up(l.bases + 8 * ranges, 16);
     l.stage = round_up(l.counts + 4 * units, 256);
     l.total = round_up(l.stage + (uint64_t)kChunk * units, 256);
     return l;
 }
 
-// Decompression / reduction workspace: control | look-back flag per stream
-// and range | zero-point offset per stream and chunk (+ total).
+// Decompression / reduction workspace, per stream: escape total per range |
+// range base | chunk prefix within its range | escape count per chunk.
 struct ScanLayout {
-    uint64_t flags, offsets, total;
+    uint64_t totals, bases, local, count, total;
 };
 ScanLayout scan_layout(uint64_t units, uint64_t S)
 {
+    const uint64_t R = S * ranges_of(units);
     ScanLayout l;
-    l.flags = kCtrlBytes;
-    l.offsets = round_up(l.flags + 8 * S * ranges_of(units), 16);
-    l.total = round_up(l.offsets + 8 * S * (units + 1), 256);
+    l.totals = kCtrlBytes;
+    l.bases = round_up(l.totals + 4 * R, 16);
+    l.local = round_up(l.bases + 8 * R, 16);
+    l.count = round_up(l.local + 4 * S * units, 16);
+    l.total = round_up(l.count + 4 * S * units, 256);
     return l;
 }
 
@@ -194,8 +199,8 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
-    a.n_flag_words = ranges;
+    a.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
+    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -228,8 +233,8 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
-    a.n_flag_words = max_ranges;
+    a.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
+    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -257,17 +262,20 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
     sc.in_bytes = in_bytes;
     sc.S = 1;
     sc.n = n;
-    sc.offsets = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.offsets);
     sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    sc.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
-    sc.n_flag_words = ranges_of(units);
+    sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
+    sc.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
+    sc.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
+    sc.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
     sc.status = d_status;
     DecompressArgs a{};
     a.in = reinterpret_cast<const uint8_t*>(d_in);
     a.in_bytes = in_bytes;
     a.out = d_out;
     a.n = n;
-    a.offsets = sc.offsets;
+    a.bases = sc.bases;
+    a.local = sc.local;
+    a.count = sc.count;
     a.status = d_status;
     return launch_decompress(sc, a, grid_for(ranges_of(units), dev->scan_per_sm, dev->sms),
                              grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
@@ -294,10 +302,11 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
     sc.in_bytes_dev = d_in_bytes;
     sc.S = S;
     sc.n = n;
-    sc.offsets = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.offsets);
     sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    sc.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.flags);
-    sc.n_flag_words = (uint64_t)S * ranges_of(units);
+    sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
+    sc.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
+    sc.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
+    sc.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
     sc.status = d_status;
     ReduceArgs a{};
     a.streams = d_streams;
@@ -305,13 +314,22 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
     a.S = S;
     a.out = d_out;
     a.n = n;
-    a.offsets = sc.offsets;
+    a.bases = sc.bases;
+    a.local = sc.local;
+    a.count = sc.count;
     a.status = d_status;
     const int per_sm = S <= kSmallShards ? dev->reduce_per_sm_small : dev->reduce_per_sm_large;
     return launch_reduce(sc, a, grid_for((uint64_t)S * ranges_of(units), dev->scan_per_sm, dev->sms),
                          grid_for(units, per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream)
+{
+    if (d_status == nullptr || !aligned(d_status, 4) || limit_us == 0 || limit_us > 1000000)
+        return ZCCL_ERR_INVALID_ARG;
+    return launch_wait_check((uint64_t)limit_us * 1000, d_status, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
 }
 
 const char* zccl_status_string(zccl_status_t s)

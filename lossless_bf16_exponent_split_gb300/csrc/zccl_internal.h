@@ -18,12 +18,12 @@ struct CompressArgs {
     zccl_segment_t single;       // the one segment when segs == nullptr
     uint32_t n_segs;
     uint32_t max_units;          // chunks the workspace has room for
-    uint32_t max_ranges;         // scan ranges (look-back flags) it has room for
+    uint32_t max_ranges;         // 32-chunk ranges it has room for
     uint8_t lut[8];
     uint64_t* out_bytes;         // device [n_segs]
     WsCtrl* ctrl;
-    uint64_t* flags;             // [max_ranges]
-    uint64_t n_flag_words;
+    uint32_t* totals;            // [max_ranges] escapes per range (zero between calls)
+    uint64_t* bases;             // [max_ranges] range offset in its stream's zero-point array
     uint32_t* counts;            // [max_units] escapes per chunk
     uint8_t* stage;              // [max_units * 4096] escapes, chunk-local
     uint32_t* status;
@@ -37,10 +37,11 @@ struct ScanArgs {
     uint64_t in_bytes;
     uint32_t S;
     uint64_t n;
-    uint64_t* offsets;           // [S][units + 1]
     WsCtrl* ctrl;
-    uint64_t* flags;             // [S][ranges per stream]
-    uint64_t n_flag_words;
+    uint32_t* totals;            // [S][ranges per stream] escapes per range
+    uint64_t* bases;             // [S][ranges per stream] range offset in its stream
+    uint32_t* local;             // [S][units] chunk offset within its range
+    uint32_t* count;             // [S][units] escapes per chunk
     uint32_t* status;
 };
 
@@ -49,7 +50,9 @@ struct DecompressArgs {
     uint64_t in_bytes;
     uint16_t* out;
     uint64_t n;
-    const uint64_t* offsets;     // [units + 1], from the scan
+    const uint64_t* bases;       // from the scan: [ranges]
+    const uint32_t* local;       // [units]
+    const uint32_t* count;       // [units]
     uint32_t* status;
 };
 
@@ -59,7 +62,9 @@ struct ReduceArgs {
     uint32_t S;
     uint16_t* out;
     uint64_t n;
-    const uint64_t* offsets;     // [S][units + 1], from the scan
+    const uint64_t* bases;       // from the scan: [S][ranges per stream]
+    const uint32_t* local;       // [S][units]
+    const uint32_t* count;       // [S][units]
     uint32_t* status;
 };
 
@@ -98,5 +103,7 @@ int decompress_ctas_per_sm();
 cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
                           cudaStream_t stream);
 int reduce_ctas_per_sm(uint32_t S);
+
+cudaError_t launch_wait_check(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 
 }  // namespace zccl

@@ -11,7 +11,8 @@
 // from stream s; a NaN sum becomes 0x7FC0.
 //
 // GB300 design: the escape scan kernel (zccl_decompress.cu) first computes
-// every shard's per-chunk zero-point offsets from the code planes; then,
+// every shard's per-chunk zero-point offsets (range base + prefix within the
+// range) from the code planes; then,
 // started by programmatic dependent launch, reduce_kernel walks the chunks
 // (persistent grid, static stride) and, for each chunk, the S shard blocks
 // in order through a 3-stage ring of shared buffers: each step is one TMA
@@ -73,11 +74,13 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
     const uint32_t units = total;
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint64_t* off = a.offsets + (uint64_t)s * (units + 1);
-    const uint64_t o0 = off[c], o1 = off[c + 1];
+    const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;
+    const uint64_t idx = (uint64_t)s * units + c;
+    const uint64_t o0 = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks) + __ldcg(a.local + idx);
+    const uint64_t o1 = o0 + __ldcg(a.count + idx);
     uint32_t zbytes = 0, delta = 0, cnt = 0;
     const uint64_t zp = zp_offset_of(a.n);
-    if (o1 >= o0 && o1 <= t.n_esc[s] && o1 - o0 <= kChunk) {
+    if (o1 <= t.n_esc[s] && o1 - o0 <= kChunk) {
         cnt = (uint32_t)(o1 - o0);
         if (cnt) {
             const uint64_t lo = zp + o0, lo16 = lo & ~15ull, hi16 = round_up(zp + o1, 16);

@@ -132,6 +132,22 @@ def test_activation_mix_full(codec):
     _full_size(codec, workloads.activation_mix(), oracle.lut_from_sigma(1.0))
 
 
+def test_shared_workspace_across_ops(codec):
+    """One workspace serves compress, decompress and reduce calls in any
+    order and size; each call must leave it ready for the next."""
+    lut = LUTS["sigma1"]
+    for i, n in enumerate([300_000, 5_000, 1_000_000, 77, 600_001]):
+        x = workloads.gaussian(n, 1.0, seed=50 + i)
+        want = oracle.compress(x, lut)
+        assert gpu_compress(codec, x, lut) == want
+        assert np.array_equal(gpu_decompress(codec, want, n), x)
+        codec.reset_status()
+        r = codec.decompress_reduce([dev_bytes(want), dev_bytes(want)], [len(want)] * 2, n)
+        torch.cuda.synchronize()
+        assert codec.read_status() == 0
+        assert np.array_equal(host_u16(r), oracle.decompress_reduce([want, want], n))
+
+
 def test_output_canary_untouched(codec):
     x = workloads.gaussian(20_000, 0.02, seed=9)
     lut = LUTS["sigma0.02"]
