@@ -49,14 +49,23 @@ __host__ __device__ inline uint64_t stream_bytes_of(uint64_t n, uint64_t n_esc)
 }
 
 // ---- workspace --------------------------------------------------------------
-// [0,128): control words (the rest of the workspace is laid out per call by
-// the host layer).
+// [0, kCtrlBytes): arrival counters (the rest of the workspace is laid out
+// per call by the host layer).  CTAs arrive in kArrivalGroups groups, each on
+// its own counter in its own 32-byte sector, and the last of each group on
+// the top counter, so no single address takes more than ~gridDim/32 atomics.
+constexpr uint32_t kArrivalGroups = 32;
 struct WsCtrl {
-    uint32_t done;  // CTAs finished in the running call; wraps to 0 at gridDim.x
-    uint32_t pad[31];
+    uint32_t top;
+    uint32_t release;  // grid-barrier generation: bumped once per barrier
+    uint32_t pad0[6];
+    struct {
+        uint32_t count;
+        uint32_t pad[7];
+    } group[kArrivalGroups];
 };
-static_assert(sizeof(WsCtrl) == 128, "control block is 128 bytes");
-constexpr uint64_t kCtrlBytes = 128;
+static_assert(sizeof(WsCtrl) == 32 * (kArrivalGroups + 1), "one 32-byte sector per counter");
+constexpr uint64_t kCtrlBytes = 2048;
+static_assert(sizeof(WsCtrl) <= kCtrlBytes, "control block fits");
 
 // Chunks per range: the unit of the per-range escape totals that one CTA
 // scans at the end of a pass.
@@ -91,9 +100,11 @@ __device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p)
     return v;
 }
 
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v)
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
 {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
@@ -112,6 +123,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
+                 : "memory");
+}
+
+// Expect `bytes` more transaction bytes in the current phase, without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
 }
 
@@ -224,20 +242,140 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // ---- last CTA of a grid --------------------------------------------------------
 // Every CTA calls this exactly once, with all its threads, after its last
 // global write of the pass.  It returns true in the one CTA that arrives
-// last, which may then read everything the others wrote; the counter wraps
-// back to 0 for the next call on the workspace.
+// last, which may then read everything the others wrote.  All counters wrap
+// back to 0 (atomicInc) for the next call on the workspace.
 __device__ inline bool arrive_last(WsCtrl* ctrl, uint32_t* s_flag)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
+        const uint32_t G = gridDim.x;
+        const uint32_t groups = G < kArrivalGroups ? G : kArrivalGroups;
+        const uint32_t g = blockIdx.x % groups;
+        const uint32_t members = (G - g + groups - 1) / groups;  // CTAs b < G with b % groups == g
         __threadfence();
-        const uint32_t old = atomicInc(&ctrl->done, gridDim.x - 1);
-        *s_flag = (old == gridDim.x - 1) ? 1u : 0u;
+        uint32_t last = 0;
+        if (atomicInc(&ctrl->group[g].count, members - 1) == members - 1) {
+            __threadfence();
+            last = atomicInc(&ctrl->top, groups - 1) == groups - 1;
+        }
+        *s_flag = last;
     }
     __syncthreads();
     const bool last = *s_flag != 0;
     if (last) __threadfence();
     return last;
+}
+
+// ---- grid barrier (cooperative launches only) ------------------------------------
+// All CTAs of a cooperatively launched grid are resident together, so they
+// may wait for one another.  `gen0` is ctrl->release read by the CTA before
+// it arrives.  The last CTA to arrive bumps ctrl->release; the others wait
+// for the bump -- a bounded wait: after kSpinTimeoutNs it returns false (the
+// caller reports ZCCL_ERR_TIMEOUT and skips the work that needed the
+// barrier).  Call with all threads; contains barriers.
+__device__ inline bool grid_barrier(WsCtrl* ctrl, uint32_t gen0, uint32_t* s_flag)
+{
+    const bool last = arrive_last(ctrl, s_flag);
+    __syncthreads();  // every thread has read *s_flag
+    if (last) {
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(&ctrl->release, 1u);
+        }
+        return true;
+    }
+    if (threadIdx.x == 0) {
+        uint32_t ok = 1;
+        if (ld_acquire_u32(&ctrl->release) == gen0) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t it = 0; ld_acquire_u32(&ctrl->release) == gen0; ++it) {
+                if ((it & 15) == 15 && globaltimer() - t0 > kSpinTimeoutNs) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        *s_flag = ok;
+    }
+    __syncthreads();
+    const bool ok = *s_flag != 0;
+    __syncthreads();
+    return ok;
+}
+
+// ---- block reductions ------------------------------------------------------------
+template <int kThreads>
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* scratch)
+{
+    v = warp_sum_u64(v);
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint64_t t = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) t += scratch[w];
+    __syncthreads();
+    return t;
+}
+
+template <int kThreads>
+__device__ __forceinline__ int64_t block_max_i64(int64_t v, int64_t* scratch)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const int64_t y = __shfl_xor_sync(0xffffffffu, v, o);
+        v = y > v ? y : v;
+    }
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int64_t t = scratch[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) t = scratch[w] > t ? scratch[w] : t;
+    __syncthreads();
+    return t;
+}
+
+// ---- segmented exclusive scan of one value per thread -------------------------
+// Thread t holds (head_t, v_t) in order t = 0..kThreads-1, after a carry-in
+// state `carry` (the sum since the last segment start before thread 0).
+// Returns sum(v) over earlier threads of t's segment (+ carry if no segment
+// start lies between thread 0 and t; 0 if head_t); *carry_out = the state
+// after the last thread.  Contains barriers.
+template <int kThreads>
+__device__ __forceinline__ uint64_t seg_block_excl_scan(bool head, uint64_t v, uint64_t carry, uint64_t* sv,
+                                                        uint32_t* sf, uint64_t* carry_out)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t f = head;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t fu = __shfl_up_sync(0xffffffffu, f, o);
+        const uint64_t xu = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) {
+            if (!f) x += xu;
+            f |= fu;
+        }
+    }
+    if (lane == 31) {
+        sf[warp] = f;
+        sv[warp] = x;
+    }
+    uint32_t fe = __shfl_up_sync(0xffffffffu, f, 1);
+    uint64_t xe = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) {
+        fe = 0;
+        xe = 0;
+    }
+    __syncthreads();
+    uint64_t px = carry;
+    for (int w = 0; w < warp; ++w) px = sf[w] ? sv[w] : px + sv[w];
+    px = fe ? xe : px + xe;
+    uint64_t tx = carry;
+    for (int w = 0; w < kThreads / 32; ++w) tx = sf[w] ? sv[w] : tx + sv[w];
+    __syncthreads();
+    *carry_out = tx;
+    return head ? 0 : px;
 }
 
 // ---- segmented exclusive scan by one CTA --------------------------------------

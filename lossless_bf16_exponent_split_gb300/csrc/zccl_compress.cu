@@ -1,6 +1,6 @@
 // zccl_compress.cu -- compression: split, remap, code planes, escape counts,
 // device-wide exclusive scan and zero-point compaction, for one stream or
-// for a batch of ragged segments.
+// for a batch of ragged segments, in one cooperative kernel.
 //
 // Page: "ZipCCL: Efficient Lossless Data Compression of Communication
 // Collectives for Accelerating LLM Training", technical summary 2.B (split
@@ -10,27 +10,27 @@
 // three independent 1-bit arrays; asynchronous global->shared copies with
 // double buffering) and 2.D (static/dynamic MoE parts -> batched segments).
 //
-// GB300 design: two kernels back to back on the caller's stream, the second
-// started by programmatic dependent launch so its launch overlaps the
-// first's tail.
+// GB300 design.  One persistent, cooperatively launched grid of 128-thread
+// CTAs (all resident at once); CTA b owns a contiguous run of the
+// 4096-element chunks (all segments' chunks in one index space).
 //
-//  compress_blocks_kernel  streams the input once.  A persistent grid of
-//    128-thread CTAs walks the 4096-element chunks; each chunk's 8 KB arrives
-//    in shared memory by a TMA bulk copy, double-buffered so the next chunk
-//    lands while this one is coded.  A thread codes 8 consecutive elements
-//    from one 16-byte shared load: byte permutes give the sign-mantissa
-//    bytes, a 256-entry shared table gives each exponent's three code bits
-//    pre-spread one byte apart, accumulated into one word whose bytes are the
-//    three plane bytes.  The coded block leaves by one bulk store.  popc over
+//  Phase 1 streams the input once.  Each chunk's 8 KB arrives in shared
+//    memory by a TMA bulk copy, double-buffered so the next chunk lands while
+//    this one is coded.  A thread codes 8 consecutive elements from one
+//    16-byte shared load: byte permutes give the sign-mantissa bytes, a
+//    256-entry shared table gives each exponent's three code bits pre-spread
+//    one byte apart, accumulated into one word whose bytes are the three
+//    plane bytes.  The coded block leaves by one bulk store.  popc over
 //    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
-//    chunk into a staging slot of the workspace, the count is recorded and
-//    added (one atomic) to its 32-chunk range's total.  No CTA waits for
-//    another: the CTA that finishes last (an atomic arrival counter) runs one
-//    segmented exclusive scan over the few hundred range totals -- the
-//    device-wide scan of the escape counts -- giving each range's base.
-//  compress_place_kernel  one CTA per range: scans its 32 counts, copies
-//    each chunk's staged escapes to base + prefix in the zero-point array,
-//    and finishes each stream (header, padding, size).
+//    chunk into a staging slot of the workspace and the count is recorded.
+//    The CTA publishes its run's escape total (since the last segment start
+//    inside the run).
+//  One grid barrier (bounded wait).
+//  Phase 2: each CTA sums the earlier runs' totals back to the last segment
+//    start -- its carry, the device-wide exclusive scan done O(grid) per CTA
+//    -- scans its own chunks' counts from there, copies each chunk's staged
+//    escapes to its place in the zero-point array and finishes the streams
+//    that end in its run (header, zero padding, size).
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -42,6 +42,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr uint32_t kInBytes = kChunk * 2;  // 8192
+constexpr uint32_t kBatch = kThreads;       // chunks placed per round in phase 2
 
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
@@ -70,14 +71,28 @@ __device__ __forceinline__ uint32_t find_segment(const uint32_t* start, uint32_t
     return lo;
 }
 
-// Per-segment chunk (and range) starts in shared memory: ustart[s] = first
-// global chunk of segment s, rstart[s] = first global range.  Invalid
-// segments get no chunks.  Returns the totals through *units, *ranges.
-// All threads; contains barriers.
-__device__ void segment_table(const CompressArgs& a, uint32_t* ustart, uint32_t* rstart, uint64_t* scan64,
-                              uint64_t* units_total, uint64_t* ranges_total)
+struct __align__(16) CompressSmem {
+    uint8_t in[2][kInBytes];   // double-buffered BF16 input chunk
+    uint8_t blk[kBlockBytes];  // coded block being assembled
+    uint32_t code_bits[256];   // exponent -> b0 | b1 << 8 | b2 << 16
+    uint64_t bar[2];
+    uint64_t scan64[kThreads / 32];
+    int64_t smax[kThreads / 32];
+    uint32_t scan[kThreads / 32];
+    uint32_t scan_f[kThreads / 32];
+    uint32_t cnt[kBatch];
+    uint64_t off[kBatch];
+    uint32_t abort;
+    uint32_t flag;
+    uint32_t gen0;
+};
+// followed by ustart[n_segs + 1]: first global chunk of each segment
+
+// Per-segment first chunk in shared memory (invalid segments get no chunks);
+// returns the total chunk count.  All threads; contains barriers.
+__device__ uint64_t segment_table(const CompressArgs& a, uint32_t* ustart, uint64_t* scan64)
 {
-    uint64_t run_u = 0, run_r = 0;
+    uint64_t run = 0;
     for (uint32_t base = 0; base < a.n_segs; base += kThreads) {
         const uint32_t s = base + threadIdx.x;
         uint64_t u = 0;
@@ -85,42 +100,17 @@ __device__ void segment_table(const CompressArgs& a, uint32_t* ustart, uint32_t*
             const zccl_segment_t d = seg_get(a, s);
             if (a.segs == nullptr || segment_error(d) == 0) u = units_of(d.n);
         }
-        const uint64_t r = (u + kRangeChunks - 1) / kRangeChunks;
-        uint64_t tot_u, tot_r;
-        const uint64_t ex_u = block_exclusive_scan<kThreads, uint64_t>(u, scan64, &tot_u);
-        const uint64_t ex_r = block_exclusive_scan<kThreads, uint64_t>(r, scan64, &tot_r);
-        if (s < a.n_segs) {
-            ustart[s] = (uint32_t)(run_u + ex_u);  // used only when the totals are in range
-            rstart[s] = (uint32_t)(run_r + ex_r);
-        }
-        run_u += tot_u;
-        run_r += tot_r;
+        uint64_t tot;
+        const uint64_t ex = block_exclusive_scan<kThreads, uint64_t>(u, scan64, &tot);
+        if (s < a.n_segs) ustart[s] = (uint32_t)(run + ex);  // used only when the total fits
+        run += tot;
     }
-    if (threadIdx.x == 0) {
-        ustart[a.n_segs] = (uint32_t)run_u;
-        rstart[a.n_segs] = (uint32_t)run_r;
-    }
-    *units_total = run_u;
-    *ranges_total = run_r;
+    if (threadIdx.x == 0) ustart[a.n_segs] = (uint32_t)run;
     __syncthreads();
+    return run;
 }
 
-// ============================================================================
-// Kernel 1: code blocks, count and stage escapes
-// ============================================================================
-struct __align__(16) BlocksSmem {
-    uint8_t in[2][kInBytes];   // double-buffered BF16 input chunk
-    uint8_t blk[kBlockBytes];  // coded block being assembled
-    uint32_t code_bits[256];   // exponent -> b0 | b1 << 8 | b2 << 16
-    uint64_t bar[2];
-    uint64_t scan64[kThreads / 32];
-    uint32_t scan[kThreads / 32];
-    uint32_t scan_f[kThreads / 32];
-    uint32_t abort;
-    uint32_t last;
-};
-
-__device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, BlocksSmem& sm,
+__device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, CompressSmem& sm,
                                                  uint32_t c, int buf)
 {
     const uint32_t s = find_segment(ustart, a.n_segs, c);
@@ -135,152 +125,6 @@ __device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const ui
         mbar_arrive(&sm.bar[buf]);
     }
 }
-
-__global__ void __launch_bounds__(kThreads) compress_blocks_kernel(const CompressArgs a)
-{
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    BlocksSmem& sm = *reinterpret_cast<BlocksSmem*>(smem_raw);
-    uint32_t* ustart = reinterpret_cast<uint32_t*>(smem_raw + sizeof(BlocksSmem));
-    uint32_t* rstart = ustart + a.n_segs + 1;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    for (int e = tid; e < 256; e += kThreads) {
-        uint32_t c = 0;
-#pragma unroll
-        for (int r = 0; r < 7; ++r)
-            if (a.lut[r] == e) c = r + 1;
-        sm.code_bits[e] = (c & 1) | (((c >> 1) & 1) << 8) | (((c >> 2) & 1) << 16);
-    }
-    uint64_t total64, ranges64;
-    segment_table(a, ustart, rstart, sm.scan64, &total64, &ranges64);
-    const bool fits = total64 <= a.max_units && ranges64 <= a.max_ranges;  // else reported by the placement kernel
-    const uint32_t total = fits ? (uint32_t)total64 : 0u;
-    if (tid == 0) {
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
-        sm.abort = 0;
-        if (blockIdx.x < total) issue_chunk_load(a, ustart, sm, blockIdx.x, 0);
-    }
-    __syncthreads();
-
-    uint32_t k = 0;
-    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
-        const int buf = k & 1;
-        if (tid == 0 && c + gridDim.x < total) issue_chunk_load(a, ustart, sm, c + gridDim.x, buf ^ 1);
-        const uint32_t s = find_segment(ustart, a.n_segs, c);
-        const zccl_segment_t d = seg_get(a, s);
-        const uint32_t cl = c - ustart[s];
-        const uint64_t first = (uint64_t)cl * kChunk;
-        const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
-        const uint32_t L = slots_of(valid);
-
-        if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
-        if (valid < kChunk) {  // tail: the last < 8 elements come by plain loads
-            const uint32_t done = valid & ~7u;
-            if (tid < (int)(valid - done))
-                reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
-        }
-        __syncthreads();
-        if (sm.abort) {  // a bulk load never landed (bounded wait ran out)
-            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
-            break;
-        }
-
-        // ---- split + remap + plane bytes: 8 elements per thread per step ----
-        const uint8_t* src = sm.in[buf];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-            if (e0 >= L) continue;
-            uint4 v = *reinterpret_cast<const uint4*>(src + 2 * e0);
-            uint32_t keep = 0xFFu;
-            if (e0 + 8 > valid) {
-                const uint32_t nv = valid > e0 ? valid - e0 : 0;  // 0..7
-                keep = (1u << nv) - 1u;
-                const uint32_t m0 = (keep & 1 ? 0x0000FFFFu : 0u) | (keep & 2 ? 0xFFFF0000u : 0u);
-                const uint32_t m1 = (keep & 4 ? 0x0000FFFFu : 0u) | (keep & 8 ? 0xFFFF0000u : 0u);
-                const uint32_t m2 = (keep & 16 ? 0x0000FFFFu : 0u) | (keep & 32 ? 0xFFFF0000u : 0u);
-                const uint32_t m3 = (keep & 64 ? 0x0000FFFFu : 0u) | (keep & 128 ? 0xFFFF0000u : 0u);
-                v = make_uint4(v.x & m0, v.y & m1, v.z & m2, v.w & m3);
-            }
-            // sign-mantissa bytes: (hi & 0x80) | (lo & 0x7F) for 4 elements at once
-            const uint32_t lo01 = __byte_perm(v.x, v.y, 0x6420), hi01 = __byte_perm(v.x, v.y, 0x7531);
-            const uint32_t lo23 = __byte_perm(v.z, v.w, 0x6420), hi23 = __byte_perm(v.z, v.w, 0x7531);
-            const uint32_t smA = (hi01 & 0x80808080u) | (lo01 & 0x7F7F7F7Fu);
-            const uint32_t smB = (hi23 & 0x80808080u) | (lo23 & 0x7F7F7F7Fu);
-            *reinterpret_cast<uint2*>(sm.blk + e0) = make_uint2(smA, smB);
-            // code bits: byte p of acc = plane p bits of the 8 elements
-            uint32_t acc = sm.code_bits[(v.x >> 7) & 0xFF];
-            acc |= sm.code_bits[(v.x >> 23) & 0xFF] << 1;
-            acc |= sm.code_bits[(v.y >> 7) & 0xFF] << 2;
-            acc |= sm.code_bits[(v.y >> 23) & 0xFF] << 3;
-            acc |= sm.code_bits[(v.z >> 7) & 0xFF] << 4;
-            acc |= sm.code_bits[(v.z >> 23) & 0xFF] << 5;
-            acc |= sm.code_bits[(v.w >> 7) & 0xFF] << 6;
-            acc |= sm.code_bits[(v.w >> 23) & 0xFF] << 7;
-            acc &= keep * 0x010101u;
-            uint8_t* planes = sm.blk + L + (e0 >> 3);
-            planes[0] = (uint8_t)acc;
-            planes[L / 8] = (uint8_t)(acc >> 8);
-            planes[L / 4] = (uint8_t)(acc >> 16);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            bulk_s2g((uint8_t*)d.out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
-            bulk_commit();
-        }
-
-        // ---- escapes: words from the planes, chunk-local compaction ----
-        uint32_t esc = 0;
-        if (tid < (int)(L / 32)) {
-            const uint32_t* pw = reinterpret_cast<const uint32_t*>(sm.blk + L);
-            const uint32_t p0 = pw[tid], p1 = pw[L / 32 + tid], p2 = pw[L / 16 + tid];
-            const uint32_t w0 = 32u * tid;
-            const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
-                                   : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-            esc = ~(p0 | p1 | p2) & vmask;
-        }
-        uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
-        uint8_t* dst = a.stage + (uint64_t)c * kChunk + excl;
-        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(src);
-        uint32_t m = esc, j = 0;
-        while (m) {
-            const uint32_t b = __ffs(m) - 1;
-            m &= m - 1;
-            dst[j++] = (uint8_t)(x16[32u * tid + b] >> 7);
-        }
-        if (tid == 0) {
-            a.counts[c] = agg;
-            if (agg) atomicAdd(&a.totals[rstart[s] + cl / kRangeChunks], agg);
-            bulk_wait_read0();
-        }
-        __syncthreads();
-    }
-    if (tid == 0) bulk_wait0();
-    pdl_launch_dependents();
-    // the last CTA: exclusive scan of the range totals within each segment
-    if (arrive_last(a.ctrl, &sm.last) && fits) {
-        const uint32_t R = (uint32_t)ranges64;
-        cta_segmented_exclusive_scan<kThreads, 2>(
-            a.totals, a.bases, R,
-            [&](uint32_t r) { return rstart[find_segment(rstart, a.n_segs, r)] == r; }, sm.scan64, sm.scan_f);
-        // leave the totals at zero for the next call
-        for (uint32_t r = tid; r < R; r += kThreads) a.totals[r] = 0;
-    }
-}
-
-// ============================================================================
-// Kernel 2: scan counts, place escapes, finish streams
-// ============================================================================
-struct __align__(16) PlaceSmem {
-    uint64_t scan64[kThreads / 32];
-    uint32_t scan[kThreads / 32];
-    uint32_t cnt[kRangeChunks];
-    uint32_t excl[kRangeChunks];
-};
 
 // Header of a finished stream (the 32 lanes of one warp write 4 bytes each).
 __device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t n_esc, const uint8_t* lut,
@@ -304,18 +148,154 @@ __device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t 
     reinterpret_cast<uint32_t*>(out)[lane] = w;
 }
 
-__global__ void __launch_bounds__(kThreads) compress_place_kernel(const CompressArgs a)
+// Codes one chunk (already in sm.in[buf]) into sm.blk, stores the block and
+// stages the escapes; returns the chunk's escape count (all threads).
+__device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSmem& sm, int buf, uint32_t c,
+                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t L = slots_of(valid);
+    const uint8_t* src = sm.in[buf];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
+        if (e0 >= L) continue;
+        uint4 v = *reinterpret_cast<const uint4*>(src + 2 * e0);
+        uint32_t keep = 0xFFu;
+        if (e0 + 8 > valid) {
+            const uint32_t nv = valid > e0 ? valid - e0 : 0;  // 0..7
+            keep = (1u << nv) - 1u;
+            const uint32_t m0 = (keep & 1 ? 0x0000FFFFu : 0u) | (keep & 2 ? 0xFFFF0000u : 0u);
+            const uint32_t m1 = (keep & 4 ? 0x0000FFFFu : 0u) | (keep & 8 ? 0xFFFF0000u : 0u);
+            const uint32_t m2 = (keep & 16 ? 0x0000FFFFu : 0u) | (keep & 32 ? 0xFFFF0000u : 0u);
+            const uint32_t m3 = (keep & 64 ? 0x0000FFFFu : 0u) | (keep & 128 ? 0xFFFF0000u : 0u);
+            v = make_uint4(v.x & m0, v.y & m1, v.z & m2, v.w & m3);
+        }
+        // sign-mantissa bytes: (hi & 0x80) | (lo & 0x7F) for 4 elements at once
+        const uint32_t lo01 = __byte_perm(v.x, v.y, 0x6420), hi01 = __byte_perm(v.x, v.y, 0x7531);
+        const uint32_t lo23 = __byte_perm(v.z, v.w, 0x6420), hi23 = __byte_perm(v.z, v.w, 0x7531);
+        const uint32_t smA = (hi01 & 0x80808080u) | (lo01 & 0x7F7F7F7Fu);
+        const uint32_t smB = (hi23 & 0x80808080u) | (lo23 & 0x7F7F7F7Fu);
+        *reinterpret_cast<uint2*>(sm.blk + e0) = make_uint2(smA, smB);
+        // code bits: byte p of acc = plane p bits of the 8 elements
+        uint32_t acc = sm.code_bits[(v.x >> 7) & 0xFF];
+        acc |= sm.code_bits[(v.x >> 23) & 0xFF] << 1;
+        acc |= sm.code_bits[(v.y >> 7) & 0xFF] << 2;
+        acc |= sm.code_bits[(v.y >> 23) & 0xFF] << 3;
+        acc |= sm.code_bits[(v.z >> 7) & 0xFF] << 4;
+        acc |= sm.code_bits[(v.z >> 23) & 0xFF] << 5;
+        acc |= sm.code_bits[(v.w >> 7) & 0xFF] << 6;
+        acc |= sm.code_bits[(v.w >> 23) & 0xFF] << 7;
+        acc &= keep * 0x010101u;
+        uint8_t* planes = sm.blk + L + (e0 >> 3);
+        planes[0] = (uint8_t)acc;
+        planes[L / 8] = (uint8_t)(acc >> 8);
+        planes[L / 4] = (uint8_t)(acc >> 16);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_s2g((uint8_t*)d.out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
+        bulk_commit();
+    }
+    // escapes: words from the planes, chunk-local compaction into the stage
+    uint32_t esc = 0;
+    if (tid < (int)(L / 32)) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(sm.blk + L);
+        const uint32_t w0 = 32u * tid;
+        const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+        esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
+    }
+    uint32_t agg;
+    const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+    uint8_t* dst = a.stage + (uint64_t)c * kChunk + excl;
+    const uint16_t* x16 = reinterpret_cast<const uint16_t*>(src);
+    uint32_t m = esc, j = 0;
+    while (m) {
+        const uint32_t b = __ffs(m) - 1;
+        m &= m - 1;
+        dst[j++] = (uint8_t)(x16[32u * tid + b] >> 7);
+    }
+    return agg;
+}
+
+__global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    PlaceSmem& sm = *reinterpret_cast<PlaceSmem*>(smem_raw);
-    uint32_t* ustart = reinterpret_cast<uint32_t*>(smem_raw + sizeof(PlaceSmem));
-    uint32_t* rstart = ustart + a.n_segs + 1;
+    CompressSmem& sm = *reinterpret_cast<CompressSmem*>(smem_raw);
+    uint32_t* ustart = reinterpret_cast<uint32_t*>(smem_raw + sizeof(CompressSmem));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t b = blockIdx.x, G = gridDim.x;
 
-    pdl_wait();  // counts, range bases and staged escapes of the blocks kernel
-    uint64_t total_units, total_ranges;
-    segment_table(a, ustart, rstart, sm.scan64, &total_units, &total_ranges);
-    if (blockIdx.x == 0 && a.segs != nullptr) {
+    for (int e = tid; e < 256; e += kThreads) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int r = 0; r < 7; ++r)
+            if (a.lut[r] == e) c = r + 1;
+        sm.code_bits[e] = (c & 1) | (((c >> 1) & 1) << 8) | (((c >> 2) & 1) << 16);
+    }
+    if (tid == 0) sm.gen0 = *(volatile uint32_t*)&a.ctrl->release;
+    const uint64_t total64 = segment_table(a, ustart, sm.scan64);
+    const bool fits = total64 <= a.max_units;
+    const uint32_t T = fits ? (uint32_t)total64 : 0u;
+    const uint32_t lo = (uint32_t)((uint64_t)T * b / G), hi = (uint32_t)((uint64_t)T * (b + 1) / G);
+
+    // ---- phase 1: code my chunks, stage escapes, count ----
+    if (tid == 0) {
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        fence_mbar_init();
+        sm.abort = 0;
+        if (lo < hi) issue_chunk_load(a, ustart, sm, lo, 0);
+    }
+    __syncthreads();
+    uint64_t run_v = 0;   // escapes since the last segment start in my run (thread 0)
+    uint32_t run_h = 0;   // a segment starts in my run
+    uint32_t k = 0;
+    for (uint32_t c = lo; c < hi; ++c, ++k) {
+        const int buf = k & 1;
+        if (tid == 0 && c + 1 < hi) issue_chunk_load(a, ustart, sm, c + 1, buf ^ 1);
+        const uint32_t s = find_segment(ustart, a.n_segs, c);
+        const zccl_segment_t d = seg_get(a, s);
+        const uint32_t cl = c - ustart[s];
+        const uint64_t first = (uint64_t)cl * kChunk;
+        const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
+        if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
+        if (valid < kChunk) {  // tail: the last < 8 elements come by plain loads
+            const uint32_t done = valid & ~7u;
+            if (tid < (int)(valid - done))
+                reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
+        }
+        __syncthreads();
+        if (sm.abort) {  // a bulk load never landed (bounded wait ran out)
+            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
+            break;
+        }
+        const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid);
+        if (tid == 0) {
+            a.counts[c] = agg;
+            if (cl == 0) {
+                run_v = 0;
+                run_h = 1;
+            }
+            run_v += agg;
+            bulk_wait_read0();
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        bulk_wait0();
+        a.part_v[b] = run_v;
+        a.part_head[b] = run_h;
+        if (sm.abort && k + 1 < hi - lo) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);  // in flight
+    }
+
+    // ---- grid barrier ----
+    if (!grid_barrier(a.ctrl, sm.gen0, &sm.flag)) {
+        if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
+        return;
+    }
+    if (b == 0 && a.segs != nullptr) {
         for (uint32_t s = tid; s < a.n_segs; s += kThreads) {
             const uint32_t bad = segment_error(a.segs[s]);
             if (bad) {
@@ -324,12 +304,12 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
             }
         }
     }
-    if (total_units > a.max_units || total_ranges > a.max_ranges) {
-        if (blockIdx.x == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
+    if (!fits) {
+        if (b == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
         return;
     }
     // empty, valid segments: header only (CTA 0)
-    if (blockIdx.x == 0) {
+    if (b == 0) {
         for (uint32_t s = warp; s < a.n_segs; s += kThreads / 32) {
             const zccl_segment_t d = seg_get(a, s);
             if (d.n != 0 || (a.segs != nullptr && segment_error(d))) continue;
@@ -337,96 +317,98 @@ __global__ void __launch_bounds__(kThreads) compress_place_kernel(const Compress
             if (lane == 0) a.out_bytes[s] = kHeaderBytes;
         }
     }
+    if (lo >= hi || sm.abort) return;
 
-    const uint32_t nr = (uint32_t)total_ranges;
-    for (uint32_t r = blockIdx.x; r < nr; r += gridDim.x) {
-        const uint32_t s = find_segment(rstart, a.n_segs, r);
-        const zccl_segment_t d = seg_get(a, s);
-        const uint32_t q = r - rstart[s];
-        const uint32_t seg_units = (uint32_t)units_of(d.n);
-        const uint32_t c0 = q * kRangeChunks;                       // first chunk, segment-local
-        const uint32_t nch = min(kRangeChunks, seg_units - c0);
-        const uint32_t g0 = ustart[s] + c0;                          // first chunk, global
-        const uint32_t cnt = tid < (int)nch ? __ldcg(a.counts + g0 + tid) : 0u;
-        uint32_t agg;
-        const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
-        if (tid < (int)kRangeChunks) {
-            sm.cnt[tid] = cnt;
-            sm.excl[tid] = ex;
+    // ---- phase 2: carry = escapes since the last segment start before my run ----
+    int64_t h = -1;
+    for (uint32_t q = tid; q < b; q += kThreads)
+        if (__ldcg(a.part_head + q)) h = q;
+    h = block_max_i64<kThreads>(h, sm.smax);
+    uint64_t part = 0;
+    for (uint32_t q = (uint32_t)(h < 0 ? 0 : h) + tid; q < b; q += kThreads) part += __ldcg(a.part_v + q);
+    uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
+
+    const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(a.stage);
+    for (uint32_t base = lo; base < hi; base += kBatch) {
+        const uint32_t nb = min(kBatch, hi - base);
+        const uint32_t c = base + tid;
+        uint32_t cnt = 0;
+        bool head = false;
+        if (tid < (int)nb) {
+            cnt = __ldcg(a.counts + c);
+            head = ustart[find_segment(ustart, a.n_segs, c)] == c;
         }
+        uint64_t carry_out;
+        const uint64_t off = seg_block_excl_scan<kThreads>(head, cnt, carry, sm.scan64, sm.scan_f, &carry_out);
+        sm.cnt[tid] = cnt;
+        sm.off[tid] = off;
         __syncthreads();
-        const uint64_t P = __ldcg(a.bases + r);
-        const uint64_t zp = zp_offset_of(d.n);
-        uint8_t* out = (uint8_t*)d.out;
-        // each warp moves 8 chunks' staged escapes: all word loads first
-        // (one memory latency), then byte stores to the unaligned target
-        constexpr int kPerWarp = kRangeChunks / (kThreads / 32);
-        const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(a.stage);
-        uint32_t v[kPerWarp];
+        // each warp moves its chunks' staged escapes, 8 chunks at a time:
+        // all word loads first (one memory latency), then byte stores
+        for (uint32_t i0 = warp; i0 < nb; i0 += 32) {
+            uint32_t v[8];
 #pragma unroll
-        for (int ii = 0; ii < kPerWarp; ++ii) {
-            const uint32_t i = warp + 4 * ii;
-            v[ii] = (i < nch && 4 * lane < sm.cnt[i]) ? __ldcg(stage32 + (uint64_t)(g0 + i) * (kChunk / 4) + lane)
-                                                       : 0u;
-        }
+            for (int ii = 0; ii < 8; ++ii) {
+                const uint32_t i = i0 + 4 * ii;
+                v[ii] = (i < nb && 4 * lane < sm.cnt[i]) ? __ldcg(stage32 + (uint64_t)(base + i) * (kChunk / 4) + lane)
+                                                        : 0u;
+            }
 #pragma unroll
-        for (int ii = 0; ii < kPerWarp; ++ii) {
-            const uint32_t i = warp + 4 * ii;
-            if (i >= nch) continue;
-            const uint32_t cnt_i = sm.cnt[i];
-            uint8_t* to = out + zp + P + sm.excl[i];
+            for (int ii = 0; ii < 8; ++ii) {
+                const uint32_t i = i0 + 4 * ii;
+                if (i >= nb) continue;
+                const uint32_t ci = base + i;
+                const uint32_t s = find_segment(ustart, a.n_segs, ci);
+                const zccl_segment_t d = seg_get(a, s);
+                const uint32_t cnt_i = sm.cnt[i];
+                const uint64_t zp = zp_offset_of(d.n);
+                uint8_t* out = (uint8_t*)d.out;
+                uint8_t* to = out + zp + sm.off[i];
 #pragma unroll
-            for (uint32_t b = 0; b < 4; ++b)
-                if (4 * lane + b < cnt_i) to[4 * lane + b] = (uint8_t)(v[ii] >> (8 * b));
-            // escape-heavy chunks: the rest, 128 bytes per round
-            for (uint32_t w = 32 + lane; 4 * w < cnt_i; w += 32) {
-                const uint32_t x = __ldcg(stage32 + (uint64_t)(g0 + i) * (kChunk / 4) + w);
+                for (uint32_t q = 0; q < 4; ++q)
+                    if (4 * lane + q < cnt_i) to[4 * lane + q] = (uint8_t)(v[ii] >> (8 * q));
+                for (uint32_t w = 32 + lane; 4 * w < cnt_i; w += 32) {  // escape-heavy chunks
+                    const uint32_t x = __ldcg(stage32 + (uint64_t)ci * (kChunk / 4) + w);
 #pragma unroll
-                for (uint32_t b = 0; b < 4; ++b)
-                    if (4 * w + b < cnt_i) to[4 * w + b] = (uint8_t)(x >> (8 * b));
+                    for (uint32_t q = 0; q < 4; ++q)
+                        if (4 * w + q < cnt_i) to[4 * w + q] = (uint8_t)(x >> (8 * q));
+                }
+                if (ci + 1 == ustart[s + 1]) {  // the segment's last chunk: finish its stream
+                    const uint64_t n_esc = sm.off[i] + cnt_i;
+                    const uint64_t pad_end = round_up(n_esc, 128);
+                    for (uint64_t p = n_esc + lane; p < pad_end; p += 32) out[zp + p] = 0;
+                    write_header(out, d.n, n_esc, a.lut, lane);
+                    if (lane == 0) a.out_bytes[s] = zp + pad_end;
+                }
             }
         }
-        if (c0 + nch == seg_units) {  // last range: header, zero padding, size
-            const uint64_t n_esc = P + agg;
-            const uint64_t pad_end = round_up(n_esc, 128);
-            for (uint64_t b = n_esc + tid; b < pad_end; b += kThreads) out[zp + b] = 0;
-            if (warp == 1) write_header(out, d.n, n_esc, a.lut, lane);
-            if (tid == 0) a.out_bytes[s] = zp + pad_end;
-        }
+        carry = carry_out;
         __syncthreads();
     }
 }
 
-template <typename K>
-int occupancy(K kernel, size_t smem)
-{
-    int blocks = 0;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess) return 1;
-    return blocks > 0 ? blocks : 1;
-}
-
 }  // namespace
 
-size_t compress_smem_bytes(uint32_t n_segs) { return sizeof(BlocksSmem) + 8ull * (n_segs + 1); }
-static size_t place_smem_bytes(uint32_t n_segs) { return sizeof(PlaceSmem) + 8ull * (n_segs + 1); }
+size_t compress_smem_bytes(uint32_t n_segs) { return sizeof(CompressSmem) + 4ull * (n_segs + 1); }
 
-cudaError_t launch_compress(const CompressArgs& a, uint32_t grid_blocks, uint32_t grid_place, cudaStream_t stream)
+cudaError_t launch_compress(const CompressArgs& a, uint32_t grid, cudaStream_t stream)
 {
-    const size_t smem1 = compress_smem_bytes(a.n_segs), smem2 = place_smem_bytes(a.n_segs);
-    cudaError_t e = cudaFuncSetAttribute(compress_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem1);
+    const size_t smem = compress_smem_bytes(a.n_segs);
+    cudaError_t e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(compress_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-    if (e != cudaSuccess) return e;
-    compress_blocks_kernel<<<grid_blocks, kThreads, smem1, stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_dependent(compress_place_kernel, grid_place, kThreads, smem2, stream, a);
+    return launch_cooperative(compress_kernel, grid, kThreads, smem, stream, a);
 }
 
-int compress_ctas_per_sm(uint32_t n_segs) { return occupancy(compress_blocks_kernel, compress_smem_bytes(n_segs)); }
-int place_ctas_per_sm(uint32_t n_segs) { return occupancy(compress_place_kernel, place_smem_bytes(n_segs)); }
+int compress_ctas_per_sm(uint32_t n_segs)
+{
+    int blocks = 0;
+    const size_t smem = compress_smem_bytes(n_segs);
+    if (cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, compress_kernel, kThreads, smem) != cudaSuccess)
+        return 1;
+    return blocks > 0 ? blocks : 1;
+}
 
 }  // namespace zccl

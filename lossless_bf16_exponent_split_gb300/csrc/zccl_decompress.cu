@@ -7,10 +7,9 @@
 // zero-point array) and 2.C (128-byte aligned blocks, three 1-bit code
 // arrays, asynchronous global->shared copies with double buffering).
 //
-// GB300 design: two kernels, the second started by programmatic dependent
-// launch.
+// GB300 design.
 //
-//  escape_scan_kernel  reads only the code planes (3/8 byte per element).
+//  escape_scan_kernel (used by the fused reduction, zccl_reduce.cu)  reads only the code planes (3/8 byte per element).
 //    One CTA per range of 32 chunks: each warp counts the escapes of 8 chunks
 //    with 16-byte loads (all issued first) and popc of ~(p0|p1|p2), and the
 //    CTA records each chunk's count and prefix within the range plus the
@@ -19,9 +18,11 @@
 //    totals -- the inverse of the encoder's device-wide scan -- and checks
 //    each stream's total against its header.  It serves S streams at once
 //    for the fused reduction.
-//  decompress_kernel  streams the blocks once: per chunk, one TMA bulk copy
-//    brings the block and a second brings the chunk's run of the zero-point
-//    array (at range base + prefix), both completing on one mbarrier,
+//  decompress_kernel  one cooperative kernel: each CTA counts the escapes
+//    of its own run of chunks from their planes, a grid barrier, then each
+//    CTA sums the earlier runs' totals and streams its chunks: per chunk,
+//    one TMA bulk copy brings the block and a second brings the chunk's run
+//    of the zero-point array, both completing on one mbarrier,
 //    double-buffered.  Escaped exponents are scattered to their element slots
 //    in shared memory; each thread rebuilds 8 consecutive elements: plane
 //    bytes spread to nibble codes, one byte permute per 4 elements looks the
@@ -188,34 +189,71 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
 }
 
 // ============================================================================
-// Kernel 2: decode
+// Decompression: one cooperative kernel
 // ============================================================================
+// CTA b owns a contiguous run of chunks.  Phase 1 counts the escapes of its
+// chunks from their code planes (plain 16-byte loads, all in flight) while
+// TMA already brings its first two blocks, and publishes the run's total.
+// After one grid barrier (bounded wait) it sums the earlier runs' totals --
+// the inverse scan done O(grid) per CTA -- and streams its chunks: per chunk
+// one bulk copy of the block and one of its zero-point run, completing on
+// one mbarrier, double-buffered.
+constexpr uint32_t kWindow = 256;  // chunk offsets kept in shared memory at once
+constexpr int kHoist = 2;          // chunks per warp whose planes are loaded at once in phase 1
+
 struct __align__(16) DecodeSmem {
     uint8_t blk[2][kBlockBytes];   // double-buffered chunk blocks
     uint8_t zpb[2][kZpBufBytes];   // the chunk's zero-point run (16-byte aligned cover)
     uint8_t expo[kChunk];          // escaped exponents at their element slot
+    uint64_t off[kWindow];         // zero-point offset of my chunks (window)
+    uint32_t cnt[kWindow];
     uint64_t bar[2];
+    uint64_t scan64[kThreads / 32];
     uint32_t zdelta[2];            // offset of the run's first byte inside zpb
-    uint32_t zcount[2];            // escapes of the chunk (from the offsets)
+    uint32_t zcount[2];            // escapes of the chunk (from the counts)
     uint32_t scan[kThreads / 32];
     uint32_t abort;
     uint32_t hdr_ok;
+    uint32_t flag;
+    uint32_t gen0;
     uint32_t lut_lo, lut_hi;
     uint64_t n_esc;
 };
 
-__device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, int buf)
+// Escape offsets of my chunks [w0, w0 + kWindow) into sm.off / sm.cnt,
+// starting at *carry; all threads; contains barriers.
+__device__ __forceinline__ void window_offsets(const DecompressArgs& a, DecodeSmem& sm, uint32_t w0, uint32_t hi,
+                                               uint64_t* carry)
+{
+    const int tid = threadIdx.x;
+    const uint32_t i0 = 2 * tid, i1 = 2 * tid + 1;
+    const uint32_t c0 = __ldcg(a.count + min(w0 + i0, hi - 1)), c1 = __ldcg(a.count + min(w0 + i1, hi - 1));
+    const uint32_t v0 = w0 + i0 < hi ? c0 : 0u, v1 = w0 + i1 < hi ? c1 : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_exclusive_scan<kThreads>(v0 + v1, sm.scan, &tot);
+    sm.off[i0] = *carry + ex;
+    sm.off[i1] = *carry + ex + v0;
+    sm.cnt[i0] = v0;
+    sm.cnt[i1] = v1;
+    *carry += tot;
+    __syncthreads();
+}
+
+// Thread 0: queue my k-th chunk c (block unless `block_done`, and its
+// zero-point run) into buffer buf.
+__device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, uint32_t k,
+                                                  int buf, bool block_done)
 {
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint64_t o0 = __ldcg(a.bases + c / kRangeChunks) + __ldcg(a.local + c);
-    const uint64_t o1 = o0 + __ldcg(a.count + c);
-    uint32_t zbytes = 0, delta = 0, cnt = 0;
-    if (o1 <= sm.n_esc && o1 - o0 <= kChunk) {  // checked against the header by the scan kernel too
-        cnt = (uint32_t)(o1 - o0);
+    const uint64_t o0 = sm.off[k % kWindow];
+    const uint32_t cnt = sm.cnt[k % kWindow];
+    uint32_t zbytes = 0, delta = 0, zc = 0;
+    if (o0 + cnt <= sm.n_esc && cnt <= kChunk) {
+        zc = cnt;
         if (cnt) {
-            const uint64_t lo = zp_offset_of(a.n) + o0, hi = zp_offset_of(a.n) + o1;
-            const uint64_t lo16 = lo & ~15ull, hi16 = round_up(hi, 16);
+            const uint64_t zp = zp_offset_of(a.n);
+            const uint64_t lo = zp + o0, lo16 = lo & ~15ull, hi16 = round_up(zp + o0 + cnt, 16);
             zbytes = (uint32_t)(hi16 - lo16);
             delta = (uint32_t)(lo - lo16);
         }
@@ -223,11 +261,11 @@ __device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, Decod
         report(a.status, ZCCL_ERR_CORRUPT_STREAM);
     }
     sm.zdelta[buf] = delta;
-    sm.zcount[buf] = cnt;
-    mbar_arrive_expect_tx(&sm.bar[buf], bytes + zbytes);
-    bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
-    if (zbytes)
-        bulk_g2s(sm.zpb[buf], a.in + ((zp_offset_of(a.n) + o0) & ~15ull), zbytes, &sm.bar[buf]);
+    sm.zcount[buf] = zc;
+    mbar_arrive_expect_tx(&sm.bar[buf], (block_done ? 0u : bytes) + zbytes);
+    if (!block_done)
+        bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
+    if (zbytes) bulk_g2s(sm.zpb[buf], a.in + ((zp_offset_of(a.n) + o0) & ~15ull), zbytes, &sm.bar[buf]);
 }
 
 __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressArgs a)
@@ -235,40 +273,106 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t total = (uint32_t)units_of(a.n);
+    const uint32_t b = blockIdx.x, G = gridDim.x;
+    const uint32_t U = (uint32_t)units_of(a.n);
+    const uint32_t lo = (uint32_t)((uint64_t)U * b / G), hi = (uint32_t)((uint64_t)U * (b + 1) / G);
+    const uint32_t mine = hi - lo;
 
-    if (tid == 0) {  // header: the scan kernel checked it too; this CTA needs its LUT
-        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
-        const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-        const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-        const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-        sm.hdr_ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
-                    zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= a.in_bytes;
+    if (tid == 0) {
+        uint64_t n_esc = 0;
+        sm.hdr_ok = stream_header_ok(a.in, a.in_bytes, a.n, &n_esc);
         sm.n_esc = n_esc;
+        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
         sm.lut_lo = h[6] << 8;
         sm.lut_hi = (h[6] >> 24) | (h[7] << 8);
+        sm.gen0 = *(volatile uint32_t*)&a.ctrl->release;
+        sm.abort = 0;
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
-        sm.abort = 0;
+        // the first two blocks need no offsets: start them now (no arrival yet)
+        for (uint32_t k = 0; k < 2 && k < mine; ++k) {
+            const uint32_t c = lo + k;
+            const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
+            const uint32_t bytes = slots_of(valid) * 11 / 8;
+            mbar_expect_tx(&sm.bar[k], bytes);
+            bulk_g2s(sm.blk[k], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[k]);
+        }
     }
-    pdl_wait();  // counts, prefixes and range bases of the scan kernel
     __syncthreads();
-    if (!sm.hdr_ok) return;  // reported by the scan kernel
-    const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
-    if (tid == 0 && blockIdx.x < total) issue_decode_load(a, sm, blockIdx.x, 0);
 
-    uint32_t k = 0;
-    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+    // ---- phase 1: escape counts of my chunks from their planes ----
+    uint32_t my_total = 0;  // per warp, lane 0
+    for (uint32_t i0 = warp; i0 < mine; i0 += kHoist * (kThreads / 32)) {
+        uint4 p[kHoist][3];
+#pragma unroll
+        for (int ii = 0; ii < kHoist; ++ii) {
+            const uint64_t c = lo + i0 + (kThreads / 32) * ii;
+            if (i0 + (kThreads / 32) * ii < mine && (c + 1) * kChunk <= a.n) {
+                const uint4* pw = reinterpret_cast<const uint4*>(a.in + kHeaderBytes + c * kBlockBytes + kChunk);
+#pragma unroll
+                for (int q = 0; q < 3; ++q) p[ii][q] = __ldg(pw + q * 32 + lane);
+            }
+        }
+#pragma unroll
+        for (int ii = 0; ii < kHoist; ++ii) {
+            const uint32_t i = i0 + (kThreads / 32) * ii;
+            const uint64_t c = lo + i;
+            if (i >= mine) continue;
+            uint32_t e;
+            if ((c + 1) * kChunk <= a.n) {
+                e = __popc(~(p[ii][0].x | p[ii][1].x | p[ii][2].x)) + __popc(~(p[ii][0].y | p[ii][1].y | p[ii][2].y)) +
+                    __popc(~(p[ii][0].z | p[ii][1].z | p[ii][2].z)) + __popc(~(p[ii][0].w | p[ii][1].w | p[ii][2].w));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            } else {  // the stream's tail chunk
+                e = warp_chunk_escapes(a.in + kHeaderBytes + c * kBlockBytes, (uint32_t)(a.n - c * kChunk));
+            }
+            if (lane == 0) {
+                a.count[c] = e;
+                my_total += e;
+            }
+        }
+    }
+    const uint64_t run_total = block_sum_u64<kThreads>(lane == 0 ? my_total : 0u, sm.scan64);
+    if (tid == 0) a.part_v[b] = run_total;
+
+    // ---- grid barrier, then my carry = escapes of all earlier runs ----
+    const bool ok = grid_barrier(a.ctrl, sm.gen0, &sm.flag);
+    if (!ok || !sm.hdr_ok) {
+        if (tid == 0) {
+            if (!ok) report(a.status, ZCCL_ERR_TIMEOUT);
+            else if (b == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            for (uint32_t k = 0; k < 2 && k < mine; ++k) {  // let the started copies land
+                mbar_arrive(&sm.bar[k]);
+                mbar_wait(&sm.bar[k], 0);
+            }
+        }
+        return;
+    }
+    uint64_t part = 0;
+    for (uint32_t q = tid; q < b; q += kThreads) part += __ldcg(a.part_v + q);
+    uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
+    const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
+
+    // ---- phase 2: stream my chunks ----
+    if (mine > 0) window_offsets(a, sm, lo, hi, &carry);
+    if (tid == 0 && mine > 0) issue_decode_load(a, sm, lo, 0, 0, true);
+    for (uint32_t k = 0; k < mine; ++k) {
+        const uint32_t c = lo + k;
         const int buf = k & 1;
-        if (tid == 0 && c + gridDim.x < total) issue_decode_load(a, sm, c + gridDim.x, buf ^ 1);
+        if ((k + 1) % kWindow == 0 && k + 1 < mine) window_offsets(a, sm, lo + k + 1, hi, &carry);
+        if (tid == 0 && k + 1 < mine) issue_decode_load(a, sm, c + 1, k + 1, buf ^ 1, k + 1 < 2);
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
         if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
         __syncthreads();
         if (sm.abort) {
-            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
+            if (tid == 0) {
+                report(a.status, ZCCL_ERR_TIMEOUT);
+                if (k + 1 < mine) mbar_wait(&sm.bar[buf ^ 1], ((k + 1) >> 1) & 1);
+            }
             break;
         }
         const uint8_t* blk = sm.blk[buf];
@@ -287,13 +391,16 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
             const uint8_t* src = sm.zpb[buf] + sm.zdelta[buf] + excl;
             uint32_t m = esc, j = 0;
             while (m) {
-                const uint32_t b = __ffs(m) - 1;
+                const uint32_t bb = __ffs(m) - 1;
                 m &= m - 1;
-                sm.expo[32u * tid + b] = src[j++];
+                sm.expo[32u * tid + bb] = src[j++];
             }
         } else if (tid == 0) {
             report(a.status, ZCCL_ERR_CORRUPT_STREAM);
         }
+        // the stream's last chunk: every escape must be accounted for
+        if (tid == 0 && c + 1 == U && sm.off[k % kWindow] + agg != sm.n_esc)
+            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
         __syncthreads();
         if (good) {
             uint16_t* dst = a.out + first;
@@ -312,11 +419,6 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
             }
         }
         __syncthreads();
-    }
-    // a load still in flight after an early stop: wait for it (bounded)
-    if (tid == 0 && sm.abort) {
-        const uint32_t c = blockIdx.x + k * gridDim.x;
-        if (c + gridDim.x < total) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);
     }
 }
 
@@ -338,15 +440,12 @@ cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_decompress(const ScanArgs& s, const DecompressArgs& a, uint32_t grid_scan, uint32_t grid,
-                              cudaStream_t stream)
+cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream)
 {
     const size_t smem = sizeof(DecodeSmem);
     cudaError_t e = cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_scan(s, grid_scan, stream);
-    if (e != cudaSuccess) return e;
-    return launch_dependent(decompress_kernel, grid, kThreads, smem, stream, a);
+    return launch_cooperative(decompress_kernel, grid, kThreads, smem, stream, a);
 }
 
 int scan_ctas_per_sm() { return occupancy(escape_scan_kernel, 0); }

@@ -27,8 +27,6 @@ struct DeviceInfo {
     int sms = 0;
     int compress_per_sm = 1;
     int compress_per_sm_batched = 1;
-    int place_per_sm = 1;
-    int place_per_sm_batched = 1;
     int scan_per_sm = 1;
     int decompress_per_sm = 1;
     int reduce_per_sm_small = 1;  // S <= kSmallShards
@@ -49,8 +47,6 @@ const DeviceInfo* device_info()
         d.sms = sms > 0 ? sms : 1;
         d.compress_per_sm = compress_ctas_per_sm(1);
         d.compress_per_sm_batched = compress_ctas_per_sm(ZCCL_MAX_SEGMENTS);
-        d.place_per_sm = place_ctas_per_sm(1);
-        d.place_per_sm_batched = place_ctas_per_sm(ZCCL_MAX_SEGMENTS);
         d.scan_per_sm = scan_ctas_per_sm();
         d.decompress_per_sm = decompress_ctas_per_sm();
         d.reduce_per_sm_small = reduce_ctas_per_sm(kSmallShards);
@@ -72,20 +68,34 @@ bool lut_ok(const zccl_lut_t* lut)
 
 uint64_t ranges_of(uint64_t units) { return (units + kRangeChunks - 1) / kRangeChunks; }
 
-// Compression workspace: control | escape total per 32-chunk range (zero
-// between calls) | range base | escape count per chunk | a 4096-byte escape
+// Compression workspace: control | escape total of each CTA's run | run
+// contains a segment start | escape count per chunk | a 4096-byte escape
 // staging slot per chunk.
 struct CompressLayout {
-    uint64_t totals, bases, counts, stage, total;
+    uint64_t part_v, part_head, counts, stage, total;
 };
-CompressLayout compress_layout(uint64_t units, uint64_t ranges)
+CompressLayout compress_layout(uint64_t units)
 {
     CompressLayout l;
-    l.totals = kCtrlBytes;
-    l.bases = round_up(l.totals + 4 * ranges, 16);
-    l.counts = round_up(l.bases + 8 * ranges, 16);
+    l.part_v = kCtrlBytes;
+    l.part_head = l.part_v + 8ull * kMaxGrid;
+    l.counts = l.part_head + 4ull * kMaxGrid;
     l.stage = round_up(l.counts + 4 * units, 256);
     l.total = round_up(l.stage + (uint64_t)kChunk * units, 256);
+    return l;
+}
+
+// Decompression workspace: control | escape total of each CTA's run |
+// escape count per chunk.
+struct DecompressLayout {
+    uint64_t part_v, count, total;
+};
+DecompressLayout decompress_layout(uint64_t units)
+{
+    DecompressLayout l;
+    l.part_v = kCtrlBytes;
+    l.count = l.part_v + 8ull * kMaxGrid;
+    l.total = round_up(l.count + 4 * units, 256);
     return l;
 }
 
@@ -107,14 +117,10 @@ ScanLayout scan_layout(uint64_t units, uint64_t S)
 }
 
 uint64_t batched_max_units(uint64_t total_n, uint32_t n_segs) { return total_n / kChunk + n_segs; }
-uint64_t batched_max_ranges(uint64_t total_n, uint32_t n_segs)
-{
-    return batched_max_units(total_n, n_segs) / kRangeChunks + n_segs;
-}
 
 uint32_t grid_for(uint64_t units, int per_sm, int sms)
 {
-    const uint64_t cap = (uint64_t)per_sm * (uint64_t)sms;
+    const uint64_t cap = std::min<uint64_t>((uint64_t)per_sm * (uint64_t)sms, kMaxGrid);
     const uint64_t g = std::min<uint64_t>(units, cap);
     return (uint32_t)std::max<uint64_t>(g, 1);
 }
@@ -153,13 +159,11 @@ zccl_status_t zccl_workspace_bytes(int op, uint64_t n, uint32_t k, uint64_t* byt
 {
     if (bytes == nullptr || n >= kMaxElems) return ZCCL_ERR_INVALID_ARG;
     switch (op) {
-        case ZCCL_OP_COMPRESS:
-            *bytes = compress_layout(units_of(n), ranges_of(units_of(n))).total;
-            return ZCCL_OK;
-        case ZCCL_OP_DECOMPRESS: *bytes = scan_layout(units_of(n), 1).total; return ZCCL_OK;
+        case ZCCL_OP_COMPRESS: *bytes = compress_layout(units_of(n)).total; return ZCCL_OK;
+        case ZCCL_OP_DECOMPRESS: *bytes = decompress_layout(units_of(n)).total; return ZCCL_OK;
         case ZCCL_OP_COMPRESS_BATCHED:
             if (k == 0 || k > ZCCL_MAX_SEGMENTS) return ZCCL_ERR_INVALID_ARG;
-            *bytes = compress_layout(batched_max_units(n, k), batched_max_ranges(n, k)).total;
+            *bytes = compress_layout(batched_max_units(n, k)).total;
             return ZCCL_OK;
         case ZCCL_OP_DECOMPRESS_REDUCE:
             if (k == 0 || k > ZCCL_MAX_SHARDS) return ZCCL_ERR_INVALID_ARG;
@@ -184,8 +188,8 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
         !aligned(d_out_bytes, 8) || d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
         return ZCCL_ERR_INVALID_ARG;
     if (out_capacity < zccl_max_compressed_bytes(n)) return ZCCL_ERR_BUFFER_TOO_SMALL;
-    const uint64_t units = units_of(n), ranges = ranges_of(units);
-    const CompressLayout l = compress_layout(units, ranges);
+    const uint64_t units = units_of(n);
+    const CompressLayout l = compress_layout(units);
     if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
@@ -195,17 +199,15 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
     a.single = zccl_segment_t{d_in, n, d_out, out_capacity};
     a.n_segs = 1;
     a.max_units = (uint32_t)units;
-    a.max_ranges = (uint32_t)ranges;
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
-    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
+    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
+    a.part_head = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.part_head);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
-    return launch_compress(a, grid_for(units, dev->compress_per_sm, dev->sms),
-                           grid_for(ranges, dev->place_per_sm, dev->sms), stream) == cudaSuccess
+    return launch_compress(a, grid_for(units, dev->compress_per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
 }
@@ -219,8 +221,7 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
         d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
         return ZCCL_ERR_INVALID_ARG;
     const uint64_t max_units = batched_max_units(total_n, n_segs);
-    const uint64_t max_ranges = batched_max_ranges(total_n, n_segs);
-    const CompressLayout l = compress_layout(max_units, max_ranges);
+    const CompressLayout l = compress_layout(max_units);
     if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
@@ -229,17 +230,15 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     a.segs = d_segs;
     a.n_segs = n_segs;
     a.max_units = (uint32_t)max_units;
-    a.max_ranges = (uint32_t)max_ranges;
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
-    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
+    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
+    a.part_head = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.part_head);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
-    return launch_compress(a, grid_for(max_units, dev->compress_per_sm_batched, dev->sms),
-                           grid_for(max_ranges, dev->place_per_sm_batched, dev->sms), stream) == cudaSuccess
+    return launch_compress(a, grid_for(max_units, dev->compress_per_sm_batched, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
 }
@@ -252,33 +251,21 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
         return ZCCL_ERR_INVALID_ARG;
     if (in_bytes < zp_offset_of(n)) return ZCCL_ERR_INVALID_ARG;
     const uint64_t units = units_of(n);
-    const ScanLayout l = scan_layout(units, 1);
+    const DecompressLayout l = decompress_layout(units);
     if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo* dev = device_info();
     if (dev == nullptr) return ZCCL_ERR_CUDA;
 
-    ScanArgs sc{};
-    sc.single = reinterpret_cast<const uint8_t*>(d_in);
-    sc.in_bytes = in_bytes;
-    sc.S = 1;
-    sc.n = n;
-    sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
-    sc.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
-    sc.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
-    sc.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
-    sc.status = d_status;
     DecompressArgs a{};
     a.in = reinterpret_cast<const uint8_t*>(d_in);
     a.in_bytes = in_bytes;
     a.out = d_out;
     a.n = n;
-    a.bases = sc.bases;
-    a.local = sc.local;
-    a.count = sc.count;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
+    a.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
     a.status = d_status;
-    return launch_decompress(sc, a, grid_for(ranges_of(units), dev->scan_per_sm, dev->sms),
-                             grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
+    return launch_decompress(a, grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
 }

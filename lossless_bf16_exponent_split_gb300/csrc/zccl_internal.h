@@ -18,12 +18,11 @@ struct CompressArgs {
     zccl_segment_t single;       // the one segment when segs == nullptr
     uint32_t n_segs;
     uint32_t max_units;          // chunks the workspace has room for
-    uint32_t max_ranges;         // 32-chunk ranges it has room for
     uint8_t lut[8];
     uint64_t* out_bytes;         // device [n_segs]
     WsCtrl* ctrl;
-    uint32_t* totals;            // [max_ranges] escapes per range (zero between calls)
-    uint64_t* bases;             // [max_ranges] range offset in its stream's zero-point array
+    uint64_t* part_v;            // [grid] escapes of each CTA's run since its last segment start
+    uint32_t* part_head;         // [grid] a segment starts inside the run
     uint32_t* counts;            // [max_units] escapes per chunk
     uint8_t* stage;              // [max_units * 4096] escapes, chunk-local
     uint32_t* status;
@@ -50,9 +49,9 @@ struct DecompressArgs {
     uint64_t in_bytes;
     uint16_t* out;
     uint64_t n;
-    const uint64_t* bases;       // from the scan: [ranges]
-    const uint32_t* local;       // [units]
-    const uint32_t* count;       // [units]
+    WsCtrl* ctrl;
+    uint64_t* part_v;            // [grid] escapes of each CTA's run
+    uint32_t* count;             // [units] escapes per chunk
     uint32_t* status;
 };
 
@@ -89,15 +88,36 @@ cudaError_t launch_dependent(void (*kernel)(Args), uint32_t grid, uint32_t threa
     return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+// Launches `kernel` cooperatively: all its CTAs are resident at once (the
+// launch fails otherwise), so they may wait for one another at a grid
+// barrier.
+template <typename Args>
+cudaError_t launch_cooperative(void (*kernel)(Args), uint32_t grid, uint32_t threads, size_t smem,
+                               cudaStream_t stream, const Args& a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Largest grid the cooperative kernels use (sizes the per-CTA workspace arrays).
+constexpr uint32_t kMaxGrid = 4096;
+
 size_t compress_smem_bytes(uint32_t n_segs);
-cudaError_t launch_compress(const CompressArgs& a, uint32_t grid_blocks, uint32_t grid_place, cudaStream_t stream);
+cudaError_t launch_compress(const CompressArgs& a, uint32_t grid, cudaStream_t stream);
 int compress_ctas_per_sm(uint32_t n_segs);
-int place_ctas_per_sm(uint32_t n_segs);
 
 cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream);
 int scan_ctas_per_sm();
-cudaError_t launch_decompress(const ScanArgs& s, const DecompressArgs& a, uint32_t grid_scan, uint32_t grid,
-                              cudaStream_t stream);
+cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream);
 int decompress_ctas_per_sm();
 
 cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
