@@ -178,6 +178,30 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
  * paper has no counterpart; it exists to test the failure path. */
 zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream);
 
+/* Size of the static device scratch used by zccl_decompress_noalloc, and the
+ * largest stream it can decode (the workspace of zccl_decompress for that n
+ * fits in the scratch). */
+#define ZCCL_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define ZCCL_NOALLOC_MAX_ELEMS 1038090240ull /* 253,440 chunks of 4096 */
+
+/* zccl_decompress for callers that cannot allocate device memory -- such as
+ * a communication library's progress thread or transport plugin, or a
+ * framework hook that must stay inside the framework's own memory pool,
+ * where a cudaMalloc could block on device-wide synchronisation, fail under
+ * a fixed memory budget or fragment the pool in the middle of a collective.
+ * The paper has no counterpart to this entry point.
+ * Same arguments and results as zccl_decompress, minus the workspace: the
+ * library uses a static device array of ZCCL_NOALLOC_SCRATCH_BYTES (1 MiB)
+ * that every GPU loading the library holds until the process exits.  n above
+ * ZCCL_NOALLOC_MAX_ELEMS returns ZCCL_ERR_INVALID_ARG and queues nothing.
+ * The array's device address is looked up on the first call made with a
+ * given device current; make that first call before any stream capture.
+ * Every call shares the array (its counters are cleared at the start of each
+ * call), so calls that overlap on the GPU -- e.g. issued on two streams --
+ * race: serialise them. */
+zccl_status_t zccl_decompress_noalloc(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n,
+                                      uint32_t* d_status, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char* zccl_status_string(zccl_status_t status);
 

@@ -25,6 +25,8 @@ OP_COMPRESS, OP_DECOMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS_REDUCE = range(4)
 MAX_SEGMENTS = 4096
 MAX_SHARDS = 1024
 CHUNK = 4096
+NOALLOC_SCRATCH_BYTES = 1 << 20
+NOALLOC_MAX_ELEMS = 1038090240
 
 LIB_PATH = _build.LIB
 _lib = None
@@ -51,6 +53,8 @@ _SIGS = {
     "zccl_decompress_reduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
                                 ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                 ctypes.c_void_p], ctypes.c_int),
+    "zccl_decompress_noalloc": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
+                                 ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_check_bounded_wait": ([ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_status_string": ([ctypes.c_int], ctypes.c_char_p),
 }
@@ -135,6 +139,12 @@ def zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes, d
                            stream) -> int:
     return lib().zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes,
                                         d_status, stream)
+
+
+def zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream) -> int:
+    """zccl_decompress without a caller workspace (static 1 MiB device
+    scratch inside the library; for callers that cannot allocate)."""
+    return lib().zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream)
 
 
 def zccl_check_bounded_wait(limit_us, d_status, stream) -> int:
