@@ -182,7 +182,7 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
  * largest stream it can decode (the workspace of zccl_decompress for that n
  * fits in the scratch). */
 #define ZCCL_NOALLOC_SCRATCH_BYTES (1u << 20)
-#define ZCCL_NOALLOC_MAX_ELEMS 1038090240ull /* 253,440 chunks of 4096 */
+#define ZCCL_NOALLOC_MAX_ELEMS 477102080ull /* 116,480 chunks of 4096 */
 
 /* zccl_decompress for callers that cannot allocate device memory -- such as
  * a communication library's progress thread or transport plugin, or a

@@ -49,21 +49,26 @@ __host__ __device__ inline uint64_t stream_bytes_of(uint64_t n, uint64_t n_esc)
 }
 
 // ---- workspace --------------------------------------------------------------
-// [0, kCtrlBytes): arrival counters (the rest of the workspace is laid out
-// per call by the host layer).  CTAs arrive in kArrivalGroups groups, each on
-// its own counter in its own 32-byte sector, and the last of each group on
-// the top counter, so no single address takes more than ~gridDim/32 atomics.
+// [0, kCtrlBytes): control words; the rest of the workspace is laid out per
+// call by the host layer.
+// Per-op state of the cooperative kernels: op_gen[op] counts completed calls
+// of that op on this workspace (bumped by the call's last CTA); a call uses
+// ticket[op][op_gen & 1] and clears the other for the next call.
+enum : uint32_t { kOpCompress = 0, kOpDecompress = 1 };
 constexpr uint32_t kArrivalGroups = 32;
 struct WsCtrl {
-    uint32_t top;
-    uint32_t release;  // grid-barrier generation: bumped once per barrier
-    uint32_t pad0[6];
+    uint32_t gen;           // grid-barrier generation, polled by waiting CTAs (own line)
+    uint32_t pad0[31];
+    uint32_t op_gen[2];
+    uint32_t ticket[2][2];
+    uint32_t pad1[26];
+    uint32_t top;           // arrivals of the group leaders (own 32-byte sector)
+    uint32_t pad2[7];
     struct {
-        uint32_t count;
+        uint32_t count;     // arrivals in group g (each in its own 32-byte sector)
         uint32_t pad[7];
     } group[kArrivalGroups];
 };
-static_assert(sizeof(WsCtrl) == 32 * (kArrivalGroups + 1), "one 32-byte sector per counter");
 constexpr uint64_t kCtrlBytes = 2048;
 static_assert(sizeof(WsCtrl) <= kCtrlBytes, "control block fits");
 
@@ -186,6 +191,11 @@ __device__ __forceinline__ void bulk_wait_read0()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// ... all but the most recent bulk-store group.
+__device__ __forceinline__ void bulk_wait_read1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Wait until the bulk stores issued by this thread are complete.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Order this thread's generic-proxy smem writes before later bulk copies.
@@ -239,69 +249,107 @@ __device__ __forceinline__ void pdl_launch_dependents()
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ---- last CTA of a grid --------------------------------------------------------
+// ---- arrival counters --------------------------------------------------------
+__device__ __forceinline__ uint32_t atom_inc_acq_rel(uint32_t* p, uint32_t wrap)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
+    return old;
+}
+
+// Thread 0 of every CTA calls this once per pass.  CTAs arrive in up to 32
+// groups, each on its own counter, and the last of each group on the top
+// counter, so no address takes more than ~gridDim/32 atomics.  Returns true
+// in the one CTA that arrives last overall.  The counters wrap back to 0
+// (atom.inc) for the next pass; acquire-release order makes everything the
+// others wrote before arriving visible to the last CTA.
+__device__ __forceinline__ bool arrive_counters(WsCtrl* ctrl)
+{
+    const uint32_t G = gridDim.x;
+    const uint32_t groups = G < kArrivalGroups ? G : kArrivalGroups;
+    const uint32_t g = blockIdx.x % groups;
+    const uint32_t members = (G - g + groups - 1) / groups;  // CTAs b < G with b % groups == g
+    if (atom_inc_acq_rel(&ctrl->group[g].count, members - 1) != members - 1) return false;
+    return atom_inc_acq_rel(&ctrl->top, groups - 1) == groups - 1;
+}
+
 // Every CTA calls this exactly once, with all its threads, after its last
-// global write of the pass.  It returns true in the one CTA that arrives
-// last, which may then read everything the others wrote.  All counters wrap
-// back to 0 (atomicInc) for the next call on the workspace.
+// global write of the pass; returns true in the one CTA that arrives last,
+// which may then read everything the others wrote.
 __device__ inline bool arrive_last(WsCtrl* ctrl, uint32_t* s_flag)
 {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t G = gridDim.x;
-        const uint32_t groups = G < kArrivalGroups ? G : kArrivalGroups;
-        const uint32_t g = blockIdx.x % groups;
-        const uint32_t members = (G - g + groups - 1) / groups;  // CTAs b < G with b % groups == g
-        __threadfence();
-        uint32_t last = 0;
-        if (atomicInc(&ctrl->group[g].count, members - 1) == members - 1) {
-            __threadfence();
-            last = atomicInc(&ctrl->top, groups - 1) == groups - 1;
-        }
-        *s_flag = last;
-    }
+    if (threadIdx.x == 0) *s_flag = arrive_counters(ctrl) ? 1u : 0u;
     __syncthreads();
-    const bool last = *s_flag != 0;
-    if (last) __threadfence();
-    return last;
+    return *s_flag != 0;
 }
 
 // ---- grid barrier (cooperative launches only) ------------------------------------
 // All CTAs of a cooperatively launched grid are resident together, so they
-// may wait for one another.  `gen0` is ctrl->release read by the CTA before
-// it arrives.  The last CTA to arrive bumps ctrl->release; the others wait
-// for the bump -- a bounded wait: after kSpinTimeoutNs it returns false (the
-// caller reports ZCCL_ERR_TIMEOUT and skips the work that needed the
-// barrier).  Call with all threads; contains barriers.
-__device__ inline bool grid_barrier(WsCtrl* ctrl, uint32_t gen0, uint32_t* s_flag)
+// may wait for one another.  A CTA reads the generation, arrives on the
+// group counters (above); the last CTA to arrive runs `last_work` (with all
+// its threads) and then publishes generation + 1 with a release store; the
+// others poll for it with back-off -- a bounded wait: after kSpinTimeoutNs
+// grid_barrier returns false (the caller reports ZCCL_ERR_TIMEOUT and skips
+// the work that needed the barrier).
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
 {
-    const bool last = arrive_last(ctrl, s_flag);
-    __syncthreads();  // every thread has read *s_flag
-    if (last) {
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(&ctrl->release, 1u);
-        }
-        return true;
-    }
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Calls of `op` completed on this workspace, as the kernel starts (only the
+// last CTA of a call changes it, after every CTA has read it).
+__device__ __forceinline__ uint32_t op_generation(const WsCtrl* ctrl, uint32_t op)
+{
+    return *(volatile const uint32_t*)&ctrl->op_gen[op];
+}
+
+template <class LastWork>
+__device__ inline bool grid_barrier(WsCtrl* ctrl, uint32_t* s_flag, LastWork last_work)
+{
+    __syncthreads();  // every thread's writes precede thread 0's release
+    uint32_t gen = 0;
     if (threadIdx.x == 0) {
-        uint32_t ok = 1;
-        if (ld_acquire_u32(&ctrl->release) == gen0) {
+        gen = *(volatile const uint32_t*)&ctrl->gen;  // cannot move before every CTA has arrived
+        uint32_t f = 2;  // 2 = last to arrive, 1 = released, 0 = timed out
+        if (!arrive_counters(ctrl)) {
+            f = 1;
             const uint64_t t0 = globaltimer();
-            for (uint32_t it = 0; ld_acquire_u32(&ctrl->release) == gen0; ++it) {
+            for (uint32_t it = 0; ld_acquire_u32(&ctrl->gen) == gen; ++it) {
                 if ((it & 15) == 15 && globaltimer() - t0 > kSpinTimeoutNs) {
-                    ok = 0;
+                    f = 0;
                     break;
                 }
-                __nanosleep(32);
+                __nanosleep(64);
             }
         }
-        *s_flag = ok;
+        *s_flag = f;
     }
     __syncthreads();
-    const bool ok = *s_flag != 0;
+    const uint32_t f = *s_flag;
     __syncthreads();
-    return ok;
+    if (f == 2u) {
+        last_work();
+        __syncthreads();
+        if (threadIdx.x == 0) st_release_u32(&ctrl->gen, gen + 1);
+        return true;
+    }
+    return f == 1u;
+}
+
+// ---- warp scans --------------------------------------------------------------------
+// Exclusive prefix sum over the 32 lanes; *total = the warp's sum.
+__device__ __forceinline__ uint32_t warp_exclusive_scan(uint32_t v, uint32_t* total)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    *total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - v;
 }
 
 // ---- block reductions ------------------------------------------------------------
@@ -333,6 +381,33 @@ __device__ __forceinline__ int64_t block_max_i64(int64_t v, int64_t* scratch)
     for (int w = 1; w < kThreads / 32; ++w) t = scratch[w] > t ? scratch[w] : t;
     __syncthreads();
     return t;
+}
+
+// ---- exclusive scan by one CTA -----------------------------------------------------
+// out[r] = in[0] + ... + in[r-1] for r < R (R <= kThreads * K per tile; larger
+// R runs tile by tile).  Loads bypass L1 (the inputs were written by other
+// CTAs); each thread's K loads are all in flight at once.  Contains barriers.
+template <int kThreads, int K>
+__device__ void cta_exclusive_scan(const uint32_t* in, uint64_t* out, uint32_t R, uint64_t* scratch)
+{
+    uint64_t carry = 0;
+    for (uint32_t base = 0; base < R; base += kThreads * K) {
+        const uint32_t first = base + threadIdx.x * K;
+        uint32_t v[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) v[j] = first + j < R ? __ldcg(in + first + j) : 0u;
+        uint64_t mine = 0;
+#pragma unroll
+        for (int j = 0; j < K; ++j) mine += v[j];
+        uint64_t tile;
+        uint64_t run = carry + block_exclusive_scan<kThreads, uint64_t>(mine, scratch, &tile);
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            if (first + j < R) out[first + j] = run;
+            run += v[j];
+        }
+        carry += tile;
+    }
 }
 
 // ---- segmented exclusive scan of one value per thread -------------------------

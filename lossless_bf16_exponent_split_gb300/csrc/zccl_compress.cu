@@ -11,26 +11,30 @@
 // double buffering) and 2.D (static/dynamic MoE parts -> batched segments).
 //
 // GB300 design.  One persistent, cooperatively launched grid of 128-thread
-// CTAs (all resident at once); CTA b owns a contiguous run of the
-// 4096-element chunks (all segments' chunks in one index space).
+// CTAs (all resident at once); all segments' 4096-element chunks form one
+// index space, cut into one contiguous run per CTA for the scan.
 //
-//  Phase 1 streams the input once.  Each chunk's 8 KB arrives in shared
-//    memory by a TMA bulk copy, double-buffered so the next chunk lands while
-//    this one is coded.  A thread codes 8 consecutive elements from one
+//  Phase 1 streams the input once.  CTAs take chunks by atomic ticket (SMs
+//    that get their data faster take more chunks).  Each chunk's 8 KB arrives
+//    in shared memory by a TMA bulk copy, double-buffered so the next chunk
+//    lands while this one is coded.  A thread codes 8 consecutive elements from one
 //    16-byte shared load: byte permutes give the sign-mantissa bytes, a
 //    256-entry shared table gives each exponent's three code bits pre-spread
 //    one byte apart, accumulated into one word whose bytes are the three
 //    plane bytes.  The coded block leaves by one bulk store.  popc over
 //    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
-//    chunk into a staging slot of the workspace and the count is recorded.
-//    The CTA publishes its run's escape total (since the last segment start
-//    inside the run).
+//    chunk into a staging slot of the workspace, the count is recorded and,
+//    if no segment starts after the chunk within its run, added to the run's
+//    accumulator (the run's escapes since its last segment start).
 //  One grid barrier (bounded wait).
-//  Phase 2: each CTA sums the earlier runs' totals back to the last segment
-//    start -- its carry, the device-wide exclusive scan done O(grid) per CTA
-//    -- scans its own chunks' counts from there, copies each chunk's staged
-//    escapes to its place in the zero-point array and finishes the streams
-//    that end in its run (header, zero padding, size).
+//  Phase 2: CTA b takes run b: it sums the accumulators of the runs back to
+//    the last segment start -- its carry, the device-wide exclusive scan done
+//    O(grid) per CTA -- scans its run's chunk counts from there, copies each
+//    chunk's staged escapes to its place in the zero-point array and
+//    finishes the streams that end in the run (header, zero padding, size).
+//  Tickets and accumulators come in two sets picked by the parity of the
+//  count of compress calls on the workspace; each call clears the set the
+//  next one will use.
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -84,7 +88,8 @@ struct __align__(16) CompressSmem {
     uint64_t off[kBatch];
     uint32_t abort;
     uint32_t flag;
-    uint32_t gen0;
+    uint32_t gen;
+    uint32_t next;  // next ticket
 };
 // followed by ustart[n_segs + 1]: first global chunk of each segment
 
@@ -219,6 +224,16 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
     return agg;
 }
 
+// Contiguous runs of the T chunks, one per CTA: run r = [run_lo(r), run_lo(r + 1)).
+__device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t G)
+{
+    return (uint32_t)(((uint64_t)r * T + G - 1) / G);
+}
+__device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t T, uint32_t G)
+{
+    return (uint32_t)((uint64_t)c * G / T);
+}
+
 __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -234,27 +249,38 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (a.lut[r] == e) c = r + 1;
         sm.code_bits[e] = (c & 1) | (((c >> 1) & 1) << 8) | (((c >> 2) & 1) << 16);
     }
-    if (tid == 0) sm.gen0 = *(volatile uint32_t*)&a.ctrl->release;
-    const uint64_t total64 = segment_table(a, ustart, sm.scan64);
+    if (tid == 0) sm.gen = op_generation(a.ctrl, kOpCompress);
+    const uint64_t total64 = segment_table(a, ustart, sm.scan64);  // (contains barriers)
     const bool fits = total64 <= a.max_units;
     const uint32_t T = fits ? (uint32_t)total64 : 0u;
-    const uint32_t lo = (uint32_t)((uint64_t)T * b / G), hi = (uint32_t)((uint64_t)T * (b + 1) / G);
+    const uint32_t par = sm.gen & 1;
+    uint32_t* tickets = &a.ctrl->ticket[kOpCompress][par];
+    uint64_t* acc = a.run_acc + (uint64_t)par * kMaxGrid;
+    {  // clear the other set for the next call
+        uint64_t* other = a.run_acc + (uint64_t)(par ^ 1) * kMaxGrid;
+        for (uint32_t i = b * kMaxGrid / G + tid; i < (b + 1) * kMaxGrid / G; i += kThreads) other[i] = 0;
+        if (b == 0 && tid == 0) a.ctrl->ticket[kOpCompress][par ^ 1] = 0;
+    }
 
-    // ---- phase 1: code my chunks, stage escapes, count ----
+    // ---- phase 1: code chunks taken by ticket, stage escapes, count ----
     if (tid == 0) {
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
         sm.abort = 0;
-        if (lo < hi) issue_chunk_load(a, ustart, sm, lo, 0);
+        const uint32_t t = atomicAdd(tickets, 1u);
+        sm.next = t;
+        if (t < T) issue_chunk_load(a, ustart, sm, t, 0);
     }
     __syncthreads();
-    uint64_t run_v = 0;   // escapes since the last segment start in my run (thread 0)
-    uint32_t run_h = 0;   // a segment starts in my run
-    uint32_t k = 0;
-    for (uint32_t c = lo; c < hi; ++c, ++k) {
+    uint32_t c = sm.next, k = 0;
+    while (c < T) {
         const int buf = k & 1;
-        if (tid == 0 && c + 1 < hi) issue_chunk_load(a, ustart, sm, c + 1, buf ^ 1);
+        if (tid == 0) {
+            const uint32_t t = atomicAdd(tickets, 1u);
+            sm.next = t;
+            if (t < T) issue_chunk_load(a, ustart, sm, t, buf ^ 1);
+        }
         const uint32_t s = find_segment(ustart, a.n_segs, c);
         const zccl_segment_t d = seg_get(a, s);
         const uint32_t cl = c - ustart[s];
@@ -274,24 +300,23 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid);
         if (tid == 0) {
             a.counts[c] = agg;
-            if (cl == 0) {
-                run_v = 0;
-                run_h = 1;
-            }
-            run_v += agg;
+            const uint32_t r = run_of(c, T, G);
+            if (agg != 0 && ustart[s + 1] >= run_lo(r + 1, T, G)) atomicAdd((unsigned long long*)&acc[r], agg);
             bulk_wait_read0();
         }
         __syncthreads();
+        c = sm.next;
+        ++k;
     }
     if (tid == 0) {
         bulk_wait0();
-        a.part_v[b] = run_v;
-        a.part_head[b] = run_h;
-        if (sm.abort && k + 1 < hi - lo) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);  // in flight
+        if (sm.abort && sm.next < T) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);  // in flight
     }
 
     // ---- grid barrier ----
-    if (!grid_barrier(a.ctrl, sm.gen0, &sm.flag)) {
+    if (!grid_barrier(a.ctrl, &sm.flag, [&] {
+            if (tid == 0) a.ctrl->op_gen[kOpCompress] = sm.gen + 1;
+        })) {
         if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
         return;
     }
@@ -317,41 +342,46 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (lane == 0) a.out_bytes[s] = kHeaderBytes;
         }
     }
+    const uint32_t lo = run_lo(b, T, G), hi = run_lo(b + 1, T, G);
     if (lo >= hi || sm.abort) return;
 
-    // ---- phase 2: carry = escapes since the last segment start before my run ----
-    int64_t h = -1;
-    for (uint32_t q = tid; q < b; q += kThreads)
-        if (__ldcg(a.part_head + q)) h = q;
-    h = block_max_i64<kThreads>(h, sm.smax);
-    uint64_t part = 0;
-    for (uint32_t q = (uint32_t)(h < 0 ? 0 : h) + tid; q < b; q += kThreads) part += __ldcg(a.part_v + q);
-    uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
-
+    // ---- phase 2: run b.  carry = escapes from the start of lo's segment ----
+    const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
+    const uint32_t h0 = st < lo ? run_of(st, T, G) : b;  // accumulators [h0, b) make the carry
     const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(a.stage);
+    uint64_t carry = 0;
     for (uint32_t base = lo; base < hi; base += kBatch) {
         const uint32_t nb = min(kBatch, hi - base);
-        const uint32_t c = base + tid;
-        uint32_t cnt = 0;
-        bool head = false;
-        if (tid < (int)nb) {
-            cnt = __ldcg(a.counts + c);
-            head = ustart[find_segment(ustart, a.n_segs, c)] == c;
+        // issue every load of the batch before using any: my chunk count,
+        // the first staged word of each of my warp's first 8 chunks, and (first
+        // batch) the accumulators of the carry
+        const uint32_t cc = base + tid;
+        const uint32_t cnt = tid < (int)nb ? __ldcg(a.counts + cc) : 0u;
+        uint32_t v[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+            const uint32_t i = warp + 4 * ii;
+            v[ii] = i < nb ? __ldcg(stage32 + (uint64_t)(base + i) * (kChunk / 4) + lane) : 0u;
         }
+        if (base == lo) {
+            uint64_t part = 0;
+            for (uint32_t q = h0 + tid; q < b; q += kThreads) part += __ldcg(acc + q);
+            carry = block_sum_u64<kThreads>(part, sm.scan64);
+        }
+        const bool head = tid < (int)nb && ustart[find_segment(ustart, a.n_segs, cc)] == cc;
         uint64_t carry_out;
         const uint64_t off = seg_block_excl_scan<kThreads>(head, cnt, carry, sm.scan64, sm.scan_f, &carry_out);
         sm.cnt[tid] = cnt;
         sm.off[tid] = off;
         __syncthreads();
-        // each warp moves its chunks' staged escapes, 8 chunks at a time:
-        // all word loads first (one memory latency), then byte stores
+        // each warp moves its chunks' staged escapes, 8 chunks at a time
         for (uint32_t i0 = warp; i0 < nb; i0 += 32) {
-            uint32_t v[8];
+            if (i0 != (uint32_t)warp) {
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
-                const uint32_t i = i0 + 4 * ii;
-                v[ii] = (i < nb && 4 * lane < sm.cnt[i]) ? __ldcg(stage32 + (uint64_t)(base + i) * (kChunk / 4) + lane)
-                                                        : 0u;
+                for (int ii = 0; ii < 8; ++ii) {
+                    const uint32_t i = i0 + 4 * ii;
+                    v[ii] = i < nb ? __ldcg(stage32 + (uint64_t)(base + i) * (kChunk / 4) + lane) : 0u;
+                }
             }
 #pragma unroll
             for (int ii = 0; ii < 8; ++ii) {

@@ -191,63 +191,65 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
 // ============================================================================
 // Decompression: one cooperative kernel
 // ============================================================================
-// CTA b owns a contiguous run of chunks.  Phase 1 counts the escapes of its
-// chunks from their code planes (plain 16-byte loads, all in flight) while
-// TMA already brings its first two blocks, and publishes the run's total.
-// After one grid barrier (bounded wait) it sums the earlier runs' totals --
-// the inverse scan done O(grid) per CTA -- and streams its chunks: per chunk
-// one bulk copy of the block and one of its zero-point run, completing on
-// one mbarrier, double-buffered.
-constexpr uint32_t kWindow = 256;  // chunk offsets kept in shared memory at once
-constexpr int kHoist = 2;          // chunks per warp whose planes are loaded at once in phase 1
+// Phase 1: CTA b counts the escapes of run b (a contiguous run of chunks,
+// one per CTA) from their code planes -- TMA bulk copies of up to 15 chunks'
+// planes at once into the still unused stream buffers, popc there -- and
+// records each chunk's count and prefix within the run, and the run total;
+// then it starts its first two chunks' block copies.  At the grid barrier (bounded wait) the last CTA to arrive scans the run totals
+// into run bases and checks the grand total against the header.  Phase 2
+// streams chunks taken by atomic ticket (SMs that get their data faster take
+// more): per chunk one bulk copy of the block and one of its zero-point run
+// (at base + prefix), completing on one mbarrier, double-buffered.
+constexpr uint32_t kPlaneBytes = kChunk * 3 / 8;  // the three planes of a full chunk: 1536 bytes
+constexpr uint32_t kPlaneSlots = 15;               // chunks whose planes fit the stream buffers at once
 
-struct __align__(16) DecodeSmem {
+struct __align__(16) DecodeSmem {  // blk, zpb and expo must stay contiguous (phase-1 slots)
     uint8_t blk[2][kBlockBytes];   // double-buffered chunk blocks
     uint8_t zpb[2][kZpBufBytes];   // the chunk's zero-point run (16-byte aligned cover)
     uint8_t expo[kChunk];          // escaped exponents at their element slot
-    uint64_t off[kWindow];         // zero-point offset of my chunks (window)
-    uint32_t cnt[kWindow];
+    uint32_t rcnt[kThreads];       // counts of a batch of my run's chunks
     uint64_t bar[2];
+    uint64_t pbar;                 // plane copies of phase 1
     uint64_t scan64[kThreads / 32];
+    uint32_t scan_f[kThreads / 32];
+    uint32_t chunk[2];             // chunk held by each buffer
     uint32_t zdelta[2];            // offset of the run's first byte inside zpb
-    uint32_t zcount[2];            // escapes of the chunk (from the counts)
+    uint32_t zcount[2];            // escapes of the chunk
     uint32_t scan[kThreads / 32];
     uint32_t abort;
     uint32_t hdr_ok;
     uint32_t flag;
-    uint32_t gen0;
+    uint32_t gen;
+    uint32_t next;
     uint32_t lut_lo, lut_hi;
     uint64_t n_esc;
 };
 
-// Escape offsets of my chunks [w0, w0 + kWindow) into sm.off / sm.cnt,
-// starting at *carry; all threads; contains barriers.
-__device__ __forceinline__ void window_offsets(const DecompressArgs& a, DecodeSmem& sm, uint32_t w0, uint32_t hi,
-                                               uint64_t* carry)
+__device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t G)
 {
-    const int tid = threadIdx.x;
-    const uint32_t i0 = 2 * tid, i1 = 2 * tid + 1;
-    const uint32_t c0 = __ldcg(a.count + min(w0 + i0, hi - 1)), c1 = __ldcg(a.count + min(w0 + i1, hi - 1));
-    const uint32_t v0 = w0 + i0 < hi ? c0 : 0u, v1 = w0 + i1 < hi ? c1 : 0u;
-    uint32_t tot;
-    const uint32_t ex = block_exclusive_scan<kThreads>(v0 + v1, sm.scan, &tot);
-    sm.off[i0] = *carry + ex;
-    sm.off[i1] = *carry + ex + v0;
-    sm.cnt[i0] = v0;
-    sm.cnt[i1] = v1;
-    *carry += tot;
-    __syncthreads();
+    return (uint32_t)(((uint64_t)r * T + G - 1) / G);
+}
+__device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t T, uint32_t G)
+{
+    return (uint32_t)((uint64_t)c * G / T);
 }
 
-// Thread 0: queue my k-th chunk c (block unless `block_done`, and its
-// zero-point run) into buffer buf.
-__device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, uint32_t k,
-                                                  int buf, bool block_done)
+// Thread 0: start the block copy of chunk c into buffer buf (no arrival).
+__device__ __forceinline__ void start_block(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, int buf)
 {
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint64_t o0 = sm.off[k % kWindow];
-    const uint32_t cnt = sm.cnt[k % kWindow];
+    sm.chunk[buf] = c;
+    mbar_expect_tx(&sm.bar[buf], bytes);
+    bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
+}
+
+// Thread 0: start the zero-point copy of the chunk in buffer buf and arrive.
+__device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm, int buf, uint32_t T, uint32_t G)
+{
+    const uint32_t c = sm.chunk[buf];
+    const uint64_t o0 = __ldcg(a.bases + run_of(c, T, G)) + __ldcg(a.local + c);
+    const uint32_t cnt = __ldcg(a.count + c);
     uint32_t zbytes = 0, delta = 0, zc = 0;
     if (o0 + cnt <= sm.n_esc && cnt <= kChunk) {
         zc = cnt;
@@ -262,107 +264,137 @@ __device__ __forceinline__ void issue_decode_load(const DecompressArgs& a, Decod
     }
     sm.zdelta[buf] = delta;
     sm.zcount[buf] = zc;
-    mbar_arrive_expect_tx(&sm.bar[buf], (block_done ? 0u : bytes) + zbytes);
-    if (!block_done)
-        bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
+    mbar_arrive_expect_tx(&sm.bar[buf], zbytes);
     if (zbytes) bulk_g2s(sm.zpb[buf], a.in + ((zp_offset_of(a.n) + o0) & ~15ull), zbytes, &sm.bar[buf]);
 }
 
-__global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressArgs a)
+__global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const DecompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t b = blockIdx.x, G = gridDim.x;
-    const uint32_t U = (uint32_t)units_of(a.n);
-    const uint32_t lo = (uint32_t)((uint64_t)U * b / G), hi = (uint32_t)((uint64_t)U * (b + 1) / G);
-    const uint32_t mine = hi - lo;
+    const uint32_t T = (uint32_t)units_of(a.n);
+    const uint32_t lo = run_lo(b, T, G), hi = run_lo(b + 1, T, G);
 
     if (tid == 0) {
+        sm.abort = 0;
+        mbar_init(&sm.bar[0], 1);
+        mbar_init(&sm.bar[1], 1);
+        mbar_init(&sm.pbar, 1);
+        fence_mbar_init();
+        sm.gen = op_generation(a.ctrl, kOpDecompress);
+    }
+    __syncthreads();
+
+    // ---- phase 1: escape counts of run b from the planes ----
+    // The planes of up to kPlaneSlots chunks come in at once by TMA bulk
+    // copies into the (not yet used) block / zero-point / exponent buffers.
+    uint8_t* slots = sm.blk[0];
+    uint64_t run_total = 0;
+    uint32_t pphase = 0;
+    for (uint32_t base = lo; base < hi; base += kThreads) {
+        const uint32_t nb = min((uint32_t)kThreads, hi - base);
+        for (uint32_t s0 = 0; s0 < nb; s0 += kPlaneSlots) {
+            const uint32_t ns = min(kPlaneSlots, nb - s0);
+            if (tid == 0) {
+                uint32_t bytes = 0;
+                for (uint32_t i = 0; i < ns; ++i)
+                    if ((uint64_t)(base + s0 + i + 1) * kChunk <= a.n) bytes += kPlaneBytes;
+                mbar_arrive_expect_tx(&sm.pbar, bytes);
+                for (uint32_t i = 0; i < ns; ++i) {
+                    const uint64_t c = base + s0 + i;
+                    if ((c + 1) * kChunk <= a.n)
+                        bulk_g2s(slots + i * kPlaneBytes, a.in + kHeaderBytes + c * kBlockBytes + kChunk, kPlaneBytes,
+                                 &sm.pbar);
+                }
+            }
+            if (!mbar_wait(&sm.pbar, pphase)) atomicExch(&sm.abort, 1u);
+            pphase ^= 1;
+            for (uint32_t i = warp; i < ns; i += kThreads / 32) {
+                const uint64_t c = base + s0 + i;
+                uint32_t e;
+                if ((c + 1) * kChunk <= a.n) {
+                    const uint4* pw = reinterpret_cast<const uint4*>(slots + i * kPlaneBytes);
+                    const uint4 p0 = pw[lane], p1 = pw[32 + lane], p2 = pw[64 + lane];
+                    e = __popc(~(p0.x | p1.x | p2.x)) + __popc(~(p0.y | p1.y | p2.y)) + __popc(~(p0.z | p1.z | p2.z)) +
+                        __popc(~(p0.w | p1.w | p2.w));
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+                } else {  // the stream's tail chunk, straight from global memory
+                    e = warp_chunk_escapes(a.in + kHeaderBytes + c * kBlockBytes, (uint32_t)(a.n - c * kChunk));
+                }
+                if (lane == 0) sm.rcnt[s0 + i] = e;
+            }
+            __syncthreads();  // the slots are free for the next batch
+        }
+        const uint32_t cnt = tid < (int)nb ? sm.rcnt[tid] : 0u;
+        uint32_t tot;
+        const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &tot);
+        if (tid < (int)nb) {
+            a.local[base + tid] = (uint32_t)(run_total + ex);
+            a.count[base + tid] = cnt;
+        }
+        run_total += tot;
+    }
+    if (tid == 0) {
+        a.run_total[b] = (uint32_t)run_total;
+        // the first two chunks (by ticket): their blocks need no offsets, so
+        // start them now (the arrival comes with their zero-point copy after
+        // the grid barrier); the header is read meanwhile
+        const uint32_t gen = sm.gen;
+        const uint32_t t = atomicAdd(&a.ctrl->ticket[kOpDecompress][gen & 1], 2u);
+        for (int i = 0; i < 2; ++i) {
+            sm.chunk[i] = t + i;
+            if (t + i < T) start_block(a, sm, t + i, i);
+        }
+        if (b == 0) a.ctrl->ticket[kOpDecompress][(gen & 1) ^ 1] = 0;  // the next call's tickets
         uint64_t n_esc = 0;
         sm.hdr_ok = stream_header_ok(a.in, a.in_bytes, a.n, &n_esc);
         sm.n_esc = n_esc;
         const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
         sm.lut_lo = h[6] << 8;
         sm.lut_hi = (h[6] >> 24) | (h[7] << 8);
-        sm.gen0 = *(volatile uint32_t*)&a.ctrl->release;
-        sm.abort = 0;
-        mbar_init(&sm.bar[0], 1);
-        mbar_init(&sm.bar[1], 1);
-        fence_mbar_init();
-        // the first two blocks need no offsets: start them now (no arrival yet)
-        for (uint32_t k = 0; k < 2 && k < mine; ++k) {
-            const uint32_t c = lo + k;
-            const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
-            const uint32_t bytes = slots_of(valid) * 11 / 8;
-            mbar_expect_tx(&sm.bar[k], bytes);
-            bulk_g2s(sm.blk[k], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[k]);
-        }
     }
     __syncthreads();
 
-    // ---- phase 1: escape counts of my chunks from their planes ----
-    uint32_t my_total = 0;  // per warp, lane 0
-    for (uint32_t i0 = warp; i0 < mine; i0 += kHoist * (kThreads / 32)) {
-        uint4 p[kHoist][3];
-#pragma unroll
-        for (int ii = 0; ii < kHoist; ++ii) {
-            const uint64_t c = lo + i0 + (kThreads / 32) * ii;
-            if (i0 + (kThreads / 32) * ii < mine && (c + 1) * kChunk <= a.n) {
-                const uint4* pw = reinterpret_cast<const uint4*>(a.in + kHeaderBytes + c * kBlockBytes + kChunk);
-#pragma unroll
-                for (int q = 0; q < 3; ++q) p[ii][q] = __ldg(pw + q * 32 + lane);
-            }
+    // ---- grid barrier; the last CTA scans the run totals into run bases ----
+    const uint64_t n_esc = sm.n_esc;
+    const bool hdr_ok = sm.hdr_ok != 0;
+    const bool ok = grid_barrier(a.ctrl, &sm.flag, [&] {
+        cta_exclusive_scan<kThreads, 16>(a.run_total, a.bases, G, sm.scan64);
+        __syncthreads();
+        if (tid == 0) {
+            if (hdr_ok && a.bases[G - 1] + __ldcg(a.run_total + G - 1) != n_esc)
+                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            a.ctrl->op_gen[kOpDecompress] = sm.gen + 1;
         }
-#pragma unroll
-        for (int ii = 0; ii < kHoist; ++ii) {
-            const uint32_t i = i0 + (kThreads / 32) * ii;
-            const uint64_t c = lo + i;
-            if (i >= mine) continue;
-            uint32_t e;
-            if ((c + 1) * kChunk <= a.n) {
-                e = __popc(~(p[ii][0].x | p[ii][1].x | p[ii][2].x)) + __popc(~(p[ii][0].y | p[ii][1].y | p[ii][2].y)) +
-                    __popc(~(p[ii][0].z | p[ii][1].z | p[ii][2].z)) + __popc(~(p[ii][0].w | p[ii][1].w | p[ii][2].w));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-            } else {  // the stream's tail chunk
-                e = warp_chunk_escapes(a.in + kHeaderBytes + c * kBlockBytes, (uint32_t)(a.n - c * kChunk));
-            }
-            if (lane == 0) {
-                a.count[c] = e;
-                my_total += e;
-            }
-        }
-    }
-    const uint64_t run_total = block_sum_u64<kThreads>(lane == 0 ? my_total : 0u, sm.scan64);
-    if (tid == 0) a.part_v[b] = run_total;
-
-    // ---- grid barrier, then my carry = escapes of all earlier runs ----
-    const bool ok = grid_barrier(a.ctrl, sm.gen0, &sm.flag);
-    if (!ok || !sm.hdr_ok) {
+    });
+    if (!ok || !hdr_ok) {
         if (tid == 0) {
             if (!ok) report(a.status, ZCCL_ERR_TIMEOUT);
             else if (b == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            for (uint32_t k = 0; k < 2 && k < mine; ++k) {  // let the started copies land
-                mbar_arrive(&sm.bar[k]);
-                mbar_wait(&sm.bar[k], 0);
+            for (int i = 0; i < 2; ++i) {  // let the started copies land
+                if (sm.chunk[i] >= T) continue;
+                mbar_arrive(&sm.bar[i]);
+                mbar_wait(&sm.bar[i], 0);
             }
         }
         return;
     }
-    uint64_t part = 0;
-    for (uint32_t q = tid; q < b; q += kThreads) part += __ldcg(a.part_v + q);
-    uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
     const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
+    uint32_t* tickets = &a.ctrl->ticket[kOpDecompress][sm.gen & 1];
 
-    // ---- phase 2: stream my chunks ----
-    if (mine > 0) window_offsets(a, sm, lo, hi, &carry);
-    if (tid == 0 && mine > 0) issue_decode_load(a, sm, lo, 0, 0, true);
-    for (uint32_t k = 0; k < mine; ++k) {
-        const uint32_t c = lo + k;
+    // ---- phase 2: stream chunks taken by ticket ----
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i)
+            if (sm.chunk[i] < T) start_zp(a, sm, i, T, G);
+    }
+    __syncthreads();
+    for (uint32_t k = 0;; ++k) {
         const int buf = k & 1;
-        if ((k + 1) % kWindow == 0 && k + 1 < mine) window_offsets(a, sm, lo + k + 1, hi, &carry);
-        if (tid == 0 && k + 1 < mine) issue_decode_load(a, sm, c + 1, k + 1, buf ^ 1, k + 1 < 2);
+        const uint32_t c = sm.chunk[buf];
+        if (c >= T) break;
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
@@ -371,7 +403,7 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
         if (sm.abort) {
             if (tid == 0) {
                 report(a.status, ZCCL_ERR_TIMEOUT);
-                if (k + 1 < mine) mbar_wait(&sm.bar[buf ^ 1], ((k + 1) >> 1) & 1);
+                if (sm.chunk[buf ^ 1] < T) mbar_wait(&sm.bar[buf ^ 1], ((k + 1) >> 1) & 1);
             }
             break;
         }
@@ -398,9 +430,6 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
         } else if (tid == 0) {
             report(a.status, ZCCL_ERR_CORRUPT_STREAM);
         }
-        // the stream's last chunk: every escape must be accounted for
-        if (tid == 0 && c + 1 == U && sm.off[k % kWindow] + agg != sm.n_esc)
-            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
         __syncthreads();
         if (good) {
             uint16_t* dst = a.out + first;
@@ -416,6 +445,15 @@ __global__ void __launch_bounds__(kThreads) decompress_kernel(const DecompressAr
                 } else {
                     store_partial(dst + e0, o, valid - e0);
                 }
+            }
+        }
+        __syncthreads();  // buffer buf (block, zero-point run, expo) is free again
+        if (tid == 0) {
+            const uint32_t t = atomicAdd(tickets, 1u);
+            sm.chunk[buf] = t;
+            if (t < T) {
+                start_block(a, sm, t, buf);
+                start_zp(a, sm, buf, T, G);
             }
         }
         __syncthreads();

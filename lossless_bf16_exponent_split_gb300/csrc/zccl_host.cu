@@ -68,33 +68,39 @@ bool lut_ok(const zccl_lut_t* lut)
 
 uint64_t ranges_of(uint64_t units) { return (units + kRangeChunks - 1) / kRangeChunks; }
 
-// Compression workspace: control | escape total of each CTA's run | run
-// contains a segment start | escape count per chunk | a 4096-byte escape
-// staging slot per chunk.
+// Every workspace starts with the same prefix: the control words, then the
+// compression run accumulators (two sets of kMaxGrid), which only
+// compression touches -- so a workspace can serve any op in any order.
+constexpr uint64_t kRunAccBytes = 2ull * 8 * kMaxGrid;
+constexpr uint64_t kPrefixBytes = kCtrlBytes + kRunAccBytes;
+
+// Compression workspace: prefix | escape count per chunk | a 4096-byte
+// escape staging slot per chunk.
 struct CompressLayout {
-    uint64_t part_v, part_head, counts, stage, total;
+    uint64_t run_acc, counts, stage, total;
 };
 CompressLayout compress_layout(uint64_t units)
 {
     CompressLayout l;
-    l.part_v = kCtrlBytes;
-    l.part_head = l.part_v + 8ull * kMaxGrid;
-    l.counts = l.part_head + 4ull * kMaxGrid;
+    l.run_acc = kCtrlBytes;
+    l.counts = kPrefixBytes;
     l.stage = round_up(l.counts + 4 * units, 256);
     l.total = round_up(l.stage + (uint64_t)kChunk * units, 256);
     return l;
 }
 
-// Decompression workspace: control | escape total of each CTA's run |
-// escape count per chunk.
+// Decompression workspace: prefix | escapes per run | run base | chunk
+// offset within its run | escapes per chunk.
 struct DecompressLayout {
-    uint64_t part_v, count, total;
+    uint64_t run_total, bases, local, count, total;
 };
 DecompressLayout decompress_layout(uint64_t units)
 {
     DecompressLayout l;
-    l.part_v = kCtrlBytes;
-    l.count = l.part_v + 8ull * kMaxGrid;
+    l.run_total = kPrefixBytes;
+    l.bases = l.run_total + 4ull * kMaxGrid;
+    l.local = l.bases + 8ull * kMaxGrid;
+    l.count = l.local + 4 * units;
     l.total = round_up(l.count + 4 * units, 256);
     return l;
 }
@@ -108,7 +114,7 @@ ScanLayout scan_layout(uint64_t units, uint64_t S)
 {
     const uint64_t R = S * ranges_of(units);
     ScanLayout l;
-    l.totals = kCtrlBytes;
+    l.totals = kPrefixBytes;
     l.bases = round_up(l.totals + 4 * R, 16);
     l.local = round_up(l.bases + 8 * R, 16);
     l.count = round_up(l.local + 4 * S * units, 16);
@@ -202,8 +208,7 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
-    a.part_head = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.part_head);
+    a.run_acc = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.run_acc);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -233,8 +238,7 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
-    a.part_head = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.part_head);
+    a.run_acc = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.run_acc);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -262,7 +266,9 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
     a.out = d_out;
     a.n = n;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.part_v = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.part_v);
+    a.run_total = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.run_total);
+    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
+    a.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
     a.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
     a.status = d_status;
     return launch_decompress(a, grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess

@@ -21,8 +21,7 @@ struct CompressArgs {
     uint8_t lut[8];
     uint64_t* out_bytes;         // device [n_segs]
     WsCtrl* ctrl;
-    uint64_t* part_v;            // [grid] escapes of each CTA's run since its last segment start
-    uint32_t* part_head;         // [grid] a segment starts inside the run
+    uint64_t* run_acc;           // [2][kMaxGrid] per-run escapes since the run's last segment start
     uint32_t* counts;            // [max_units] escapes per chunk
     uint8_t* stage;              // [max_units * 4096] escapes, chunk-local
     uint32_t* status;
@@ -50,7 +49,9 @@ struct DecompressArgs {
     uint16_t* out;
     uint64_t n;
     WsCtrl* ctrl;
-    uint64_t* part_v;            // [grid] escapes of each CTA's run
+    uint32_t* run_total;         // [grid] escapes of each CTA's run
+    uint64_t* bases;             // [grid] each run's offset into the zero-point array
+    uint32_t* local;             // [units] chunk offset within its run
     uint32_t* count;             // [units] escapes per chunk
     uint32_t* status;
 };
