@@ -69,18 +69,23 @@ def source_sha(names):
     return h.hexdigest()[:16]
 
 
-# each op = two launches of the kernels in these sources (plus zccl_common.cuh)
+# the kernels of each op live in these sources (plus zccl_common.cuh)
 KERNEL_SOURCES = {"compress": ["zccl_compress.cu"], "decompress": ["zccl_decompress.cu", "zccl_decode.cuh"],
                   "decompress_reduce": ["zccl_reduce.cu", "zccl_decompress.cu", "zccl_decode.cuh"]}
-OP_KERNELS = {"compress": "compress_blocks_kernel + compress_place_kernel",
-              "decompress": "escape_scan_kernel + decompress_kernel",
-              "decompress_reduce": "escape_scan_kernel + reduce_kernel"}
+OP_KERNELS = {"compress": "compress_kernel (one cooperative launch)",
+              "decompress": "decompress_kernel (one cooperative launch)",
+              "decompress_reduce": "escape_scan_kernel + reduce_kernel (PDL pair)"}
+OP_LAUNCHES = {"compress": 1, "decompress": 1, "decompress_reduce": 2}
+# the committed ncu summary of each op's dominant kernel is
+# profiles/<PROFILE_KERNEL[op]>_<workload>.md
+PROFILE_KERNEL = {"compress": "compress_kernel", "decompress": "decompress_kernel",
+                  "decompress_reduce": "reduce_kernel"}
 
 
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken
     on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{PROFILE_KERNEL[kernel]}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -311,8 +316,6 @@ def main():
     def tdev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
 
-    launches_per_step = 0
-    kern = {}
     if kind == "roundtrip":
         n = host.size
         R = 3
@@ -337,7 +340,6 @@ def main():
             comp(r)
         torch.cuda.synchronize()
         stream_bytes = int(nbs[0].item())
-        launches_per_step = 4
         names = ["compress", "decompress"]
         alg = {"compress": 2 * n + stream_bytes, "decompress": stream_bytes + 2 * n}
         step_input_bytes = 2 * 2 * n
@@ -380,7 +382,6 @@ def main():
         comp()
         torch.cuda.synchronize()
         sb = int(nb.sum().item())
-        launches_per_step = 2
         names = ["compress"]
         alg = {"compress": 2 * total_n + sb}
         step_input_bytes = 2 * total_n
@@ -417,7 +418,6 @@ def main():
         def red():
             z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n, ws.data_ptr(),
                                              wsb, st_ptr, h), "decompress_reduce")
-        launches_per_step = 2
         names = ["decompress_reduce"]
         alg = {"decompress_reduce": sum(sizes_h) + 2 * n}
         step_input_bytes = 2 * S * n
@@ -520,7 +520,7 @@ def main():
                      "traffic": ncu_traffic(dom, args.workload),
                      "algorithmic_bytes_per_launch": alg[dom]},
         "kernels": kernels,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": sum(OP_LAUNCHES[nm] for nm in names) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
