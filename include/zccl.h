@@ -182,7 +182,7 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
  * largest stream it can decode (the workspace of zccl_decompress for that n
  * fits in the scratch). */
 #define ZCCL_NOALLOC_SCRATCH_BYTES (1u << 20)
-#define ZCCL_NOALLOC_MAX_ELEMS 477102080ull /* 116,480 chunks of 4096 */
+#define ZCCL_NOALLOC_MAX_ELEMS 502267904ull /* 122,624 chunks of 4096 */
 
 /* zccl_decompress for callers that cannot allocate device memory -- such as
  * a communication library's progress thread or transport plugin, or a
@@ -196,9 +196,9 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
  * ZCCL_NOALLOC_MAX_ELEMS returns ZCCL_ERR_INVALID_ARG and queues nothing.
  * The array's device address is looked up on the first call made with a
  * given device current; make that first call before any stream capture.
- * Every call shares the array (its counters are cleared at the start of each
- * call), so calls that overlap on the GPU -- e.g. issued on two streams --
- * race: serialise them. */
+ * Every call shares the array (the part the call uses is cleared at the
+ * start of each call), so calls that overlap on the GPU -- e.g. issued on two
+ * streams -- race: serialise them. */
 zccl_status_t zccl_decompress_noalloc(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n,
                                       uint32_t* d_status, cudaStream_t stream);
 

@@ -26,7 +26,7 @@ MAX_SEGMENTS = 4096
 MAX_SHARDS = 1024
 CHUNK = 4096
 NOALLOC_SCRATCH_BYTES = 1 << 20
-NOALLOC_MAX_ELEMS = 477102080
+NOALLOC_MAX_ELEMS = 502267904
 
 LIB_PATH = _build.LIB
 _lib = None

@@ -1,8 +1,8 @@
 // zccl_common.cuh -- device-side building blocks shared by the codec kernels:
-// stream geometry, sm_90+/sm_103a PTX wrappers (1-D bulk copies through the
-// TMA engine, mbarriers, acquire/release flags, %globaltimer), block scans and
-// the single-pass decoupled look-back that turns per-chunk escape counts into
-// zero-point offsets (the device-wide exclusive scan of the codec).
+// stream geometry, the workspace control block and its per-call parity,
+// sm_90+/sm_103a PTX wrappers (1-D bulk copies through the TMA engine,
+// mbarriers, relaxed and acquire flags, %globaltimer), flag polling with a
+// bounded wait, and block scans.
 //
 // Page: "ZipCCL: Efficient Lossless Data Compression of Communication
 // Collectives for Accelerating LLM Training", technical summary 2.B
@@ -49,21 +49,36 @@ __host__ __device__ inline uint64_t stream_bytes_of(uint64_t n, uint64_t n_esc)
 }
 
 // ---- workspace --------------------------------------------------------------
-// [0, kCtrlBytes): control words; the rest of the workspace is laid out per
-// call by the host layer.
-// Per-op state of the cooperative kernels: op_gen[op] counts completed calls
-// of that op on this workspace (bumped by the call's last CTA); a call uses
-// ticket[op][op_gen & 1] and clears the other for the next call.
-enum : uint32_t { kOpCompress = 0, kOpDecompress = 1 };
+// [0, kCtrlBytes): control words, then the flag area (two sets of kMaxGrid
+// 64-bit words, one per call parity); the rest of the workspace is laid out
+// per call by the host layer.
+//
+// Calls of the compress and decompress kernels on one workspace alternate
+// between the two flag sets by the parity of `calls`: a call reads `calls`
+// as it starts (without waiting for the value), and once it has the value
+// uses flag set (calls & 1) and done[calls & 1], and clears the other set
+// and the other done counter for the next call.  Every CTA adds to
+// done[calls & 1] after it has used the value; the CTA whose add completes
+// the call's count (all CTAs have read `calls` by then) advances `calls`.
+// Decompression draws chunk tickets from dticket[calls & 1] (it knows the
+// parity by then) and clears the other one; compression draws them from one
+// counter before it knows the parity: every CTA draws until it gets one
+// past the last chunk and then stops, so a call makes exactly chunks + CTAs
+// draws, and the CTA that drew the last of them resets the counter.  Calls
+// on one workspace run in stream order, so a call never sees another call's
+// state.
 constexpr uint32_t kArrivalGroups = 32;
 struct WsCtrl {
-    uint32_t gen;           // grid-barrier generation, polled by waiting CTAs (own line)
+    uint32_t calls;         // compress/decompress calls made on this workspace
     uint32_t pad0[31];
-    uint32_t op_gen[2];
-    uint32_t ticket[2][2];
-    uint32_t pad1[26];
+    uint32_t ticket;        // compress: chunk tickets of the running call
+    uint32_t pad2[31];
+    uint32_t dticket[2];    // decompress: chunk tickets, by call parity
+    uint32_t pad5[30];
+    uint32_t done[2];       // progress count of the running call, by call parity
+    uint32_t pad4[30];
     uint32_t top;           // arrivals of the group leaders (own 32-byte sector)
-    uint32_t pad2[7];
+    uint32_t pad3[7];
     struct {
         uint32_t count;     // arrivals in group g (each in its own 32-byte sector)
         uint32_t pad[7];
@@ -71,6 +86,12 @@ struct WsCtrl {
 };
 constexpr uint64_t kCtrlBytes = 2048;
 static_assert(sizeof(WsCtrl) <= kCtrlBytes, "control block fits");
+constexpr uint32_t kFlagWords = 4096;  // per parity; one per CTA of the largest grid
+constexpr uint64_t kFlagBytes = 2ull * 8 * kFlagWords;
+constexpr uint64_t kPrefixBytes = kCtrlBytes + kFlagBytes;
+
+// A published 64-bit flag word: bit 63 set, the value in the low bits.
+constexpr uint64_t kValid = 1ull << 63;
 
 // Chunks per range: the unit of the per-range escape totals that one CTA
 // scans at the end of a pass.
@@ -110,6 +131,49 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p)
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Polls *p until `ready(value)` holds, with back-off; gives up after
+// kSpinTimeoutNs.  Returns the last value read; *ok is false on timeout.
+template <class Ready>
+__device__ __forceinline__ uint64_t poll_u64(const uint64_t* p, Ready ready, bool* ok)
+{
+    uint64_t v = ld_relaxed_u64(p);
+    if (ready(v)) return v;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        __nanosleep(32);
+        v = ld_relaxed_u64(p);
+        if (ready(v)) return v;
+        if ((it & 15) == 15 && globaltimer() - t0 > kSpinTimeoutNs) {
+            *ok = false;
+            return v;
+        }
+    }
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
@@ -284,57 +348,67 @@ __device__ inline bool arrive_last(WsCtrl* ctrl, uint32_t* s_flag)
     return *s_flag != 0;
 }
 
-// ---- grid barrier (cooperative launches only) ------------------------------------
-// All CTAs of a cooperatively launched grid are resident together, so they
-// may wait for one another.  A CTA reads the generation, arrives on the
-// group counters (above); the last CTA to arrive runs `last_work` (with all
-// its threads) and then publishes generation + 1 with a release store; the
-// others poll for it with back-off -- a bounded wait: after kSpinTimeoutNs
-// grid_barrier returns false (the caller reports ZCCL_ERR_TIMEOUT and skips
-// the work that needed the barrier).
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
+// ---- call parity (compress / decompress) -------------------------------------
+// Thread 0 of every CTA, first thing: starts reading `calls` (the value is
+// used only later, so the load does not hold the CTA up).
+__device__ __forceinline__ uint32_t call_read(const WsCtrl* ctrl)
 {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    return ld_relaxed_u32(&ctrl->calls);
 }
 
-// Calls of `op` completed on this workspace, as the kernel starts (only the
-// last CTA of a call changes it, after every CTA has read it).
-__device__ __forceinline__ uint32_t op_generation(const WsCtrl* ctrl, uint32_t op)
+// Thread 0 of the CTA whose add completed the call's done count: advances
+// `calls` for the next call on the workspace.
+__device__ __forceinline__ void call_end(WsCtrl* ctrl, uint32_t calls, bool last)
 {
-    return *(volatile const uint32_t*)&ctrl->op_gen[op];
+    if (last) st_relaxed_u32(&ctrl->calls, calls + 1);
 }
 
-template <class LastWork>
-__device__ inline bool grid_barrier(WsCtrl* ctrl, uint32_t* s_flag, LastWork last_work)
+// Thread 0 (compress): chunk tickets from one counter.  draw_ticket starts
+// a draw; the value is consumed (with consume_ticket) only when needed, so
+// the atomic's round trip does not stall the thread.  A CTA stops drawing
+// after it consumes its first ticket >= T, so a call makes exactly
+// T + gridDim.x draws; the one that drew the last resets the counter.
+__device__ __forceinline__ uint32_t draw_ticket(WsCtrl* ctrl) { return atomicAdd(&ctrl->ticket, 1u); }
+__device__ __forceinline__ uint32_t consume_ticket(WsCtrl* ctrl, uint32_t t, uint32_t T)
 {
-    __syncthreads();  // every thread's writes precede thread 0's release
-    uint32_t gen = 0;
-    if (threadIdx.x == 0) {
-        gen = *(volatile const uint32_t*)&ctrl->gen;  // cannot move before every CTA has arrived
-        uint32_t f = 2;  // 2 = last to arrive, 1 = released, 0 = timed out
-        if (!arrive_counters(ctrl)) {
-            f = 1;
-            const uint64_t t0 = globaltimer();
-            for (uint32_t it = 0; ld_acquire_u32(&ctrl->gen) == gen; ++it) {
-                if ((it & 15) == 15 && globaltimer() - t0 > kSpinTimeoutNs) {
-                    f = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        *s_flag = f;
+    if (t == T + gridDim.x - 1) st_relaxed_u32(&ctrl->ticket, 0u);
+    return t;
+}
+
+// All threads: clear this CTA's share of the other parity's flag set (and,
+// in CTA 0, the other parity's done counter) for the next call.
+__device__ __forceinline__ void clear_other_parity(WsCtrl* ctrl, uint64_t* flags, uint32_t par)
+{
+    const uint32_t b = blockIdx.x, G = gridDim.x;
+    uint64_t* other = flags + (uint64_t)(par ^ 1) * kFlagWords;
+    for (uint32_t i = b * kFlagWords / G + threadIdx.x; i < (b + 1) * kFlagWords / G; i += blockDim.x) other[i] = 0;
+    if (b == 0 && threadIdx.x == 0) {
+        ctrl->done[par ^ 1] = 0;
+        ctrl->dticket[par ^ 1] = 0;
     }
-    __syncthreads();
-    const uint32_t f = *s_flag;
-    __syncthreads();
-    if (f == 2u) {
-        last_work();
-        __syncthreads();
-        if (threadIdx.x == 0) st_release_u32(&ctrl->gen, gen + 1);
-        return true;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Thread 0 only: waits (with back-off, bounded) until *p >= target; false
+// on timeout.  One poller per CTA keeps the polled line from flooding L2.
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target)
+{
+    uint32_t ns = 64;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_relaxed_u32(p) >= target) return true;
+        if ((it & 7) == 7 && globaltimer() - t0 > kSpinTimeoutNs) return false;
+        __nanosleep(ns);
+        if (ns < 512) ns <<= 1;
     }
-    return f == 1u;
 }
 
 // ---- warp scans --------------------------------------------------------------------

@@ -11,30 +11,34 @@
 // double buffering) and 2.D (static/dynamic MoE parts -> batched segments).
 //
 // GB300 design.  One persistent, cooperatively launched grid of 128-thread
-// CTAs (all resident at once); all segments' 4096-element chunks form one
-// index space, cut into one contiguous run per CTA for the scan.
+// CTAs; all segments' 4096-element chunks form one index space, cut into one
+// contiguous run per CTA for the scan.  No CTA ever waits for the whole grid.
 //
 //  Phase 1 streams the input once.  CTAs take chunks by atomic ticket (SMs
 //    that get their data faster take more chunks).  Each chunk's 8 KB arrives
 //    in shared memory by a TMA bulk copy, double-buffered so the next chunk
-//    lands while this one is coded.  A thread codes 8 consecutive elements from one
-//    16-byte shared load: byte permutes give the sign-mantissa bytes, a
-//    256-entry shared table gives each exponent's three code bits pre-spread
-//    one byte apart, accumulated into one word whose bytes are the three
-//    plane bytes.  The coded block leaves by one bulk store.  popc over
+//    lands while this one is coded.  A thread codes 8 consecutive elements
+//    from one 16-byte shared load: byte permutes give the sign-mantissa
+//    bytes, a 256-entry shared table gives each exponent's three code bits
+//    pre-spread one byte apart, accumulated into one word whose bytes are the
+//    three plane bytes.  The coded block leaves by one bulk store.  popc over
 //    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
-//    chunk into a staging slot of the workspace, the count is recorded and,
-//    if no segment starts after the chunk within its run, added to the run's
-//    accumulator (the run's escapes since its last segment start).
-//  One grid barrier (bounded wait).
-//  Phase 2: CTA b takes run b: it sums the accumulators of the runs back to
-//    the last segment start -- its carry, the device-wide exclusive scan done
-//    O(grid) per CTA -- scans its run's chunk counts from there, copies each
-//    chunk's staged escapes to its place in the zero-point array and
-//    finishes the streams that end in the run (header, zero padding, size).
-//  Tickets and accumulators come in two sets picked by the parity of the
-//  count of compress calls on the workspace; each call clears the set the
-//  next one will use.
+//    chunk into a staging slot of the workspace, the count is recorded, and
+//    the chunk is added to its run's flag word (one coded chunk, plus its
+//    escapes unless a segment starts after it within its run).  When the CTA
+//    runs out of tickets, thread 0 counts the CTA's chunks (and the CTA) on
+//    the call's done counter with one release add.
+//  Phase 2: once every chunk is coded (thread 0 of each CTA polls the
+//    counter), CTA b takes run b: the escapes on the flag words of the runs
+//    back to its segment's start are its carry (the device-wide exclusive
+//    scan done O(grid) per CTA).  It
+//    scans its run's chunk counts from there, copies each chunk's staged
+//    escapes to their place in the zero-point array (clearing the staging
+//    words), and finishes the streams that end in the run (header, zero
+//    padding, size).
+//  The run flag words and the counter come in two sets picked by the parity
+//  of the call count of the workspace; each call clears the set the next
+//  one will use.
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -87,9 +91,9 @@ struct __align__(16) CompressSmem {
     uint32_t cnt[kBatch];
     uint64_t off[kBatch];
     uint32_t abort;
-    uint32_t flag;
-    uint32_t gen;
-    uint32_t next;  // next ticket
+    uint32_t par;
+    uint32_t next[2];  // the chunk of iteration k + 1, in next[(k + 1) & 1]: slow threads
+                       // still read one slot while thread 0 fills the other
 };
 // followed by ustart[n_segs + 1]: first global chunk of each segment
 
@@ -234,6 +238,11 @@ __device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t T, uint32_t G)
     return (uint32_t)((uint64_t)c * G / T);
 }
 
+// A run's flag word: chunks of the run coded so far << 40 | the escapes of
+// those chunks that carry into the next run.
+constexpr uint32_t kDoneShift = 40;
+constexpr uint64_t kDoneOne = 1ull << kDoneShift;
+
 __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -242,6 +251,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t b = blockIdx.x, G = gridDim.x;
 
+    uint32_t calls = 0;    // thread 0: read now, used once the first chunk is coded
+    uint32_t coded = 0;    // thread 0: chunks this CTA coded
+    bool last = false;     // thread 0: this CTA completed the call's done count
+    if (tid == 0) calls = call_read(a.ctrl);
     for (int e = tid; e < 256; e += kThreads) {
         uint32_t c = 0;
 #pragma unroll
@@ -249,18 +262,9 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (a.lut[r] == e) c = r + 1;
         sm.code_bits[e] = (c & 1) | (((c >> 1) & 1) << 8) | (((c >> 2) & 1) << 16);
     }
-    if (tid == 0) sm.gen = op_generation(a.ctrl, kOpCompress);
     const uint64_t total64 = segment_table(a, ustart, sm.scan64);  // (contains barriers)
     const bool fits = total64 <= a.max_units;
     const uint32_t T = fits ? (uint32_t)total64 : 0u;
-    const uint32_t par = sm.gen & 1;
-    uint32_t* tickets = &a.ctrl->ticket[kOpCompress][par];
-    uint64_t* acc = a.run_acc + (uint64_t)par * kMaxGrid;
-    {  // clear the other set for the next call
-        uint64_t* other = a.run_acc + (uint64_t)(par ^ 1) * kMaxGrid;
-        for (uint32_t i = b * kMaxGrid / G + tid; i < (b + 1) * kMaxGrid / G; i += kThreads) other[i] = 0;
-        if (b == 0 && tid == 0) a.ctrl->ticket[kOpCompress][par ^ 1] = 0;
-    }
 
     // ---- phase 1: code chunks taken by ticket, stage escapes, count ----
     if (tid == 0) {
@@ -268,18 +272,18 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
         sm.abort = 0;
-        const uint32_t t = atomicAdd(tickets, 1u);
-        sm.next = t;
+        const uint32_t t = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
+        sm.next[0] = t;
         if (t < T) issue_chunk_load(a, ustart, sm, t, 0);
     }
     __syncthreads();
-    uint32_t c = sm.next, k = 0;
+    uint32_t c = sm.next[0], k = 0;
     while (c < T) {
         const int buf = k & 1;
-        if (tid == 0) {
-            const uint32_t t = atomicAdd(tickets, 1u);
-            sm.next = t;
-            if (t < T) issue_chunk_load(a, ustart, sm, t, buf ^ 1);
+        if (tid == 0) {  // the next chunk (the load of this one is in flight)
+            const uint32_t tn = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
+            sm.next[(k + 1) & 1] = tn;
+            if (tn < T) issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
         }
         const uint32_t s = find_segment(ustart, a.n_segs, c);
         const zccl_segment_t d = seg_get(a, s);
@@ -300,26 +304,31 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid);
         if (tid == 0) {
             a.counts[c] = agg;
+            // the chunk's escapes carry into the next run unless its segment
+            // ends inside this run
             const uint32_t r = run_of(c, T, G);
-            if (agg != 0 && ustart[s + 1] >= run_lo(r + 1, T, G)) atomicAdd((unsigned long long*)&acc[r], agg);
+            const uint32_t carry = ustart[s + 1] >= run_lo(r + 1, T, G) ? agg : 0u;
+            uint64_t* acc = a.flags + (uint64_t)(calls & 1) * kFlagWords;
+            atomicAdd((unsigned long long*)&acc[r], kDoneOne | carry);
+            ++coded;
             bulk_wait_read0();
         }
         __syncthreads();
-        c = sm.next;
+        c = sm.next[(k + 1) & 1];
         ++k;
     }
-    if (tid == 0) {
-        bulk_wait0();
-        if (sm.abort && sm.next < T) mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);  // in flight
-    }
+    if (tid == 0 && sm.abort && sm.next[(k + 1) & 1] < T)
+        mbar_wait(&sm.bar[(k & 1) ^ 1], ((k + 1) >> 1) & 1);  // a load still in flight
+    // Count this CTA's chunks (and the CTA itself) done: thread 0's release
+    // add, after a barrier, orders everything the CTA wrote before it (its
+    // counts, staged escapes and flag-word adds) ahead of the count.
+    if (tid == 0) sm.par = calls & 1;
+    __syncthreads();
+    const uint32_t par = sm.par;
+    if (tid == 0) last = atom_add_release_u32(&a.ctrl->done[par], coded + 1) + coded + 1 == T + G;
+    clear_other_parity(a.ctrl, a.flags, par);
+    const uint64_t* acc = a.flags + (uint64_t)par * kFlagWords;
 
-    // ---- grid barrier ----
-    if (!grid_barrier(a.ctrl, &sm.flag, [&] {
-            if (tid == 0) a.ctrl->op_gen[kOpCompress] = sm.gen + 1;
-        })) {
-        if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
-        return;
-    }
     if (b == 0 && a.segs != nullptr) {
         for (uint32_t s = tid; s < a.n_segs; s += kThreads) {
             const uint32_t bad = segment_error(a.segs[s]);
@@ -331,6 +340,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     }
     if (!fits) {
         if (b == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
+        if (tid == 0) {
+            bulk_wait0();
+            call_end(a.ctrl, calls, last);
+        }
         return;
     }
     // empty, valid segments: header only (CTA 0)
@@ -343,18 +356,47 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         }
     }
     const uint32_t lo = run_lo(b, T, G), hi = run_lo(b + 1, T, G);
-    if (lo >= hi || sm.abort) return;
+    if (lo >= hi || sm.abort) {
+        if (tid == 0) {
+            bulk_wait0();
+            call_end(a.ctrl, calls, last);
+        }
+        return;
+    }
 
     // ---- phase 2: run b.  carry = escapes from the start of lo's segment ----
+    // Once every chunk is coded (thread 0 polls the call's counter), the
+    // escapes on the flag words of runs [h0, b) are the carry.
+    if (tid == 0) {
+        const bool ok = wait_count(&a.ctrl->done[par], T + G);
+        fence_acq_rel_gpu();  // what the coders wrote before counting themselves done
+        if (!ok) sm.abort = 1;
+    }
+    __syncthreads();
+    if (sm.abort) {
+        if (tid == 0) {
+            report(a.status, ZCCL_ERR_TIMEOUT);
+            bulk_wait0();
+            call_end(a.ctrl, calls, last);
+        }
+        return;
+    }
     const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
-    const uint32_t h0 = st < lo ? run_of(st, T, G) : b;  // accumulators [h0, b) make the carry
-    const uint32_t* stage32 = reinterpret_cast<const uint32_t*>(a.stage);
-    uint64_t carry = 0;
+    const uint32_t h0 = st < lo ? run_of(st, T, G) : b;  // flag words [h0, b) make the carry
+    uint64_t part = 0;
+    for (uint32_t q0 = h0 + tid; q0 < b; q0 += 8 * kThreads) {  // all loads of a round in flight at once
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = q0 + j * kThreads < b ? __ldcg(acc + q0 + j * kThreads) : 0ull;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part += v[j] & (kDoneOne - 1);
+    }
+    uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
+    uint32_t* stage32 = reinterpret_cast<uint32_t*>(a.stage);
     for (uint32_t base = lo; base < hi; base += kBatch) {
         const uint32_t nb = min(kBatch, hi - base);
-        // issue every load of the batch before using any: my chunk count,
-        // the first staged word of each of my warp's first 8 chunks, and (first
-        // batch) the accumulators of the carry
+        // issue every load of the batch before using any: my chunk count and
+        // the first staged word of each of my warp's first 8 chunks
         const uint32_t cc = base + tid;
         const uint32_t cnt = tid < (int)nb ? __ldcg(a.counts + cc) : 0u;
         uint32_t v[8];
@@ -363,18 +405,15 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             const uint32_t i = warp + 4 * ii;
             v[ii] = i < nb ? __ldcg(stage32 + (uint64_t)(base + i) * (kChunk / 4) + lane) : 0u;
         }
-        if (base == lo) {
-            uint64_t part = 0;
-            for (uint32_t q = h0 + tid; q < b; q += kThreads) part += __ldcg(acc + q);
-            carry = block_sum_u64<kThreads>(part, sm.scan64);
-        }
         const bool head = tid < (int)nb && ustart[find_segment(ustart, a.n_segs, cc)] == cc;
         uint64_t carry_out;
         const uint64_t off = seg_block_excl_scan<kThreads>(head, cnt, carry, sm.scan64, sm.scan_f, &carry_out);
         sm.cnt[tid] = cnt;
         sm.off[tid] = off;
+        if (tid < (int)nb) a.counts[cc] = 0;  // its one reader is done with it
         __syncthreads();
-        // each warp moves its chunks' staged escapes, 8 chunks at a time
+        // each warp moves its chunks' staged escapes, 8 chunks at a time, and
+        // clears the staging words it read
         for (uint32_t i0 = warp; i0 < nb; i0 += 32) {
             if (i0 != (uint32_t)warp) {
 #pragma unroll
@@ -394,14 +433,19 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
                 const uint64_t zp = zp_offset_of(d.n);
                 uint8_t* out = (uint8_t*)d.out;
                 uint8_t* to = out + zp + sm.off[i];
+                uint32_t* from = stage32 + (uint64_t)ci * (kChunk / 4);
+                if (4 * lane < cnt_i) {
 #pragma unroll
-                for (uint32_t q = 0; q < 4; ++q)
-                    if (4 * lane + q < cnt_i) to[4 * lane + q] = (uint8_t)(v[ii] >> (8 * q));
+                    for (uint32_t q = 0; q < 4; ++q)
+                        if (4 * lane + q < cnt_i) to[4 * lane + q] = (uint8_t)(v[ii] >> (8 * q));
+                    from[lane] = 0;
+                }
                 for (uint32_t w = 32 + lane; 4 * w < cnt_i; w += 32) {  // escape-heavy chunks
-                    const uint32_t x = __ldcg(stage32 + (uint64_t)ci * (kChunk / 4) + w);
+                    const uint32_t x = __ldcg(from + w);
 #pragma unroll
                     for (uint32_t q = 0; q < 4; ++q)
                         if (4 * w + q < cnt_i) to[4 * w + q] = (uint8_t)(x >> (8 * q));
+                    from[w] = 0;
                 }
                 if (ci + 1 == ustart[s + 1]) {  // the segment's last chunk: finish its stream
                     const uint64_t n_esc = sm.off[i] + cnt_i;
@@ -414,6 +458,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         }
         carry = carry_out;
         __syncthreads();
+    }
+    if (tid == 0) {
+        bulk_wait0();  // the chunk blocks' bulk stores are written
+        call_end(a.ctrl, calls, last);
     }
 }
 

@@ -18,17 +18,19 @@
 //    totals -- the inverse of the encoder's device-wide scan -- and checks
 //    each stream's total against its header.  It serves S streams at once
 //    for the fused reduction.
-//  decompress_kernel  one cooperative kernel: each CTA counts the escapes
-//    of its own run of chunks from their planes, a grid barrier, then each
-//    CTA sums the earlier runs' totals and streams its chunks: per chunk,
-//    one TMA bulk copy brings the block and a second brings the chunk's run
-//    of the zero-point array, both completing on one mbarrier,
-//    double-buffered.  Escaped exponents are scattered to their element slots
-//    in shared memory; each thread rebuilds 8 consecutive elements: plane
-//    bytes spread to nibble codes, one byte permute per 4 elements looks the
-//    codes up in the LUT (two registers), another makes the escape mask, and
-//    byte permutes interleave sign-mantissa and exponent bytes into BF16,
-//    stored with one 16-byte write.
+//  decompress_kernel  one cooperative kernel with no grid barrier: each CTA
+//    counts the escapes of its own run of chunks from their planes and
+//    publishes the run total as a flag word, sums the earlier runs' totals
+//    itself, and publishes each of its chunks' zero-point offset and count as
+//    a flag word; then CTAs stream chunks taken by ticket: per chunk, one TMA
+//    bulk copy brings the block and a second brings the chunk's run of the
+//    zero-point array, both completing on one mbarrier, double-buffered.
+//    Escaped exponents are scattered to their element slots in shared
+//    memory; each thread rebuilds 8 consecutive elements: plane bytes spread
+//    to nibble codes, one byte permute per 4 elements looks the codes up in
+//    the LUT (two registers), another makes the escape mask, and byte
+//    permutes interleave sign-mantissa and exponent bytes into BF16, stored
+//    with one 16-byte write.
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -189,38 +191,42 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
 }
 
 // ============================================================================
-// Decompression: one cooperative kernel
+// Decompression: one cooperative kernel, no grid barrier
 // ============================================================================
-// Phase 1: CTA b counts the escapes of run b (a contiguous run of chunks,
-// one per CTA) from their code planes -- TMA bulk copies of up to 15 chunks'
+// Phase 1: CTA b counts the escapes of run b (a contiguous run of chunks, one
+// per CTA) from their code planes -- TMA bulk copies of up to 15 chunks'
 // planes at once into the still unused stream buffers, popc there -- and
-// records each chunk's count and prefix within the run, and the run total;
-// then it starts its first two chunks' block copies.  At the grid barrier (bounded wait) the last CTA to arrive scans the run totals
-// into run bases and checks the grand total against the header.  Phase 2
-// streams chunks taken by atomic ticket (SMs that get their data faster take
-// more): per chunk one bulk copy of the block and one of its zero-point run
-// (at base + prefix), completing on one mbarrier, double-buffered.
+// publishes the run's total as a flag word.  It then sums the totals of the
+// runs before it (each CTA reads them itself: no CTA waits for the whole
+// grid) and publishes, per chunk of its run, one entry word: flag | zero-point
+// offset << 13 | escape count.  Phase 2 streams chunks taken by atomic ticket
+// (SMs that get their data faster take more): per chunk one bulk copy of the
+// block and one of its run of the zero-point array, completing on one
+// mbarrier, double-buffered; the chunk's entry is read (and cleared) one
+// iteration ahead, and the next ticket is drawn one iteration ahead, so
+// neither round trip stalls the CTA.
 constexpr uint32_t kPlaneBytes = kChunk * 3 / 8;  // the three planes of a full chunk: 1536 bytes
 constexpr uint32_t kPlaneSlots = 15;               // chunks whose planes fit the stream buffers at once
+constexpr uint32_t kCountBits = 13;                // entry word: escapes (<= 4096) in the low 13 bits
 
 struct __align__(16) DecodeSmem {  // blk, zpb and expo must stay contiguous (phase-1 slots)
     uint8_t blk[2][kBlockBytes];   // double-buffered chunk blocks
     uint8_t zpb[2][kZpBufBytes];   // the chunk's zero-point run (16-byte aligned cover)
     uint8_t expo[kChunk];          // escaped exponents at their element slot
-    uint32_t rcnt[kThreads];       // counts of a batch of my run's chunks
+    uint32_t hdr[kHeaderBytes / 4];  // the stream header
+    uint64_t rloc[kThreads];       // last batch of my run: chunk offset within the run
+    uint32_t rcnt[kThreads];       //                      escapes per chunk
     uint64_t bar[2];
     uint64_t pbar;                 // plane copies of phase 1
+    uint64_t hbar;                 // header copy
     uint64_t scan64[kThreads / 32];
-    uint32_t scan_f[kThreads / 32];
     uint32_t chunk[2];             // chunk held by each buffer
     uint32_t zdelta[2];            // offset of the run's first byte inside zpb
     uint32_t zcount[2];            // escapes of the chunk
     uint32_t scan[kThreads / 32];
     uint32_t abort;
     uint32_t hdr_ok;
-    uint32_t flag;
-    uint32_t gen;
-    uint32_t next;
+    uint32_t par;
     uint32_t lut_lo, lut_hi;
     uint64_t n_esc;
 };
@@ -229,29 +235,40 @@ __device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t G)
 {
     return (uint32_t)(((uint64_t)r * T + G - 1) / G);
 }
-__device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t T, uint32_t G)
+
+// The header checks of stream_header_ok, on a copy of the header.
+__device__ __forceinline__ bool header_words_ok(const uint32_t* h, uint64_t in_bytes, uint64_t n,
+                                                uint64_t* n_esc_out)
 {
-    return (uint32_t)((uint64_t)c * G / T);
+    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+    const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
+    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+    *n_esc_out = n_esc;
+    return h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == n && zp == zp_offset_of(n) &&
+           n_esc <= n && zp + round_up(n_esc, 128) <= in_bytes;
 }
+
+__device__ __forceinline__ bool entry_ready(uint64_t e) { return (e & kValid) != 0; }
 
 // Thread 0: start the block copy of chunk c into buffer buf (no arrival).
 __device__ __forceinline__ void start_block(const DecompressArgs& a, DecodeSmem& sm, uint32_t c, int buf)
 {
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    sm.chunk[buf] = c;
     mbar_expect_tx(&sm.bar[buf], bytes);
     bulk_g2s(sm.blk[buf], a.in + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[buf]);
 }
 
-// Thread 0: start the zero-point copy of the chunk in buffer buf and arrive.
-__device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm, int buf, uint32_t T, uint32_t G)
+// Thread 0: clear chunk c's entry (its one reader is done with it), start
+// the copy of its zero-point run into buffer buf and arrive.
+__device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm, int buf, uint32_t c, uint64_t e)
 {
-    const uint32_t c = sm.chunk[buf];
-    const uint64_t o0 = __ldcg(a.bases + run_of(c, T, G)) + __ldcg(a.local + c);
-    const uint32_t cnt = __ldcg(a.count + c);
+    a.entry[c] = 0;
+    const uint64_t o0 = (e & ~kValid) >> kCountBits;
+    const uint32_t cnt = (uint32_t)(e & ((1u << kCountBits) - 1));
+    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     uint32_t zbytes = 0, delta = 0, zc = 0;
-    if (o0 + cnt <= sm.n_esc && cnt <= kChunk) {
+    if (o0 + cnt <= sm.n_esc && cnt <= valid) {
         zc = cnt;
         if (cnt) {
             const uint64_t zp = zp_offset_of(a.n);
@@ -277,13 +294,18 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
     const uint32_t T = (uint32_t)units_of(a.n);
     const uint32_t lo = run_lo(b, T, G), hi = run_lo(b + 1, T, G);
 
+    uint32_t calls = 0;
+    uint32_t published = 0;  // thread 0: run totals published before mine (compared only at exit)
     if (tid == 0) {
+        calls = call_read(a.ctrl);  // used after phase 1
         sm.abort = 0;
         mbar_init(&sm.bar[0], 1);
         mbar_init(&sm.bar[1], 1);
         mbar_init(&sm.pbar, 1);
+        mbar_init(&sm.hbar, 1);
         fence_mbar_init();
-        sm.gen = op_generation(a.ctrl, kOpDecompress);
+        mbar_arrive_expect_tx(&sm.hbar, kHeaderBytes);  // the header, read while phase 1 runs
+        bulk_g2s(sm.hdr, a.in, kHeaderBytes, &sm.hbar);
     }
     __syncthreads();
 
@@ -332,65 +354,125 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
         uint32_t tot;
         const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &tot);
         if (tid < (int)nb) {
-            a.local[base + tid] = (uint32_t)(run_total + ex);
-            a.count[base + tid] = cnt;
+            const uint64_t loc = run_total + ex;
+            if (base + kThreads < hi) {  // an earlier batch: park it in the entry (no flag yet)
+                a.entry[base + tid] = (loc << kCountBits) | cnt;
+            } else {
+                sm.rloc[tid] = loc;
+                sm.rcnt[tid] = cnt;
+            }
         }
         run_total += tot;
+        __syncthreads();
     }
     if (tid == 0) {
-        a.run_total[b] = (uint32_t)run_total;
-        // the first two chunks (by ticket): their blocks need no offsets, so
-        // start them now (the arrival comes with their zero-point copy after
-        // the grid barrier); the header is read meanwhile
-        const uint32_t gen = sm.gen;
-        const uint32_t t = atomicAdd(&a.ctrl->ticket[kOpDecompress][gen & 1], 2u);
-        for (int i = 0; i < 2; ++i) {
-            sm.chunk[i] = t + i;
-            if (t + i < T) start_block(a, sm, t + i, i);
-        }
-        if (b == 0) a.ctrl->ticket[kOpDecompress][(gen & 1) ^ 1] = 0;  // the next call's tickets
+        bool ok = mbar_wait(&sm.hbar, 0);
         uint64_t n_esc = 0;
-        sm.hdr_ok = stream_header_ok(a.in, a.in_bytes, a.n, &n_esc);
+        ok = ok && header_words_ok(sm.hdr, a.in_bytes, a.n, &n_esc);
+        sm.hdr_ok = ok && !sm.abort;
         sm.n_esc = n_esc;
-        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.in);
-        sm.lut_lo = h[6] << 8;
-        sm.lut_hi = (h[6] >> 24) | (h[7] << 8);
+        sm.lut_lo = sm.hdr[6] << 8;
+        sm.lut_hi = (sm.hdr[6] >> 24) | (sm.hdr[7] << 8);
+        const uint32_t par = calls & 1;
+        sm.par = par;
+        if (sm.hdr_ok) {
+            st_relaxed_u64(a.flags + (uint64_t)par * kFlagWords + b, kValid | run_total);
+            // a hint for the pollers (the flag bit decides), and the call's
+            // completion count: the last to publish advances `calls`
+            published = atomicAdd(&a.ctrl->done[par], 1u);
+            // the first two chunks (by ticket): their blocks need no offsets,
+            // so start them now; the arrival comes with their zero-point copy
+            const uint32_t t = atomicAdd(&a.ctrl->dticket[par], 2u);
+            for (int i = 0; i < 2; ++i) {
+                sm.chunk[i] = t + i;
+                if (t + i < T) start_block(a, sm, t + i, i);
+            }
+        } else {
+            if (sm.abort) report(a.status, ZCCL_ERR_TIMEOUT);
+            else if (b == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+        }
     }
     __syncthreads();
+    const uint32_t par = sm.par;
+    uint64_t* flags = a.flags + (uint64_t)par * kFlagWords;
+    clear_other_parity(a.ctrl, a.flags, par);
+    if (!sm.hdr_ok) {
+        if (tid == 0) call_end(a.ctrl, calls, sm.hdr_ok && published == G - 1);
+        return;
+    }
 
-    // ---- grid barrier; the last CTA scans the run totals into run bases ----
-    const uint64_t n_esc = sm.n_esc;
-    const bool hdr_ok = sm.hdr_ok != 0;
-    const bool ok = grid_barrier(a.ctrl, &sm.flag, [&] {
-        cta_exclusive_scan<kThreads, 16>(a.run_total, a.bases, G, sm.scan64);
-        __syncthreads();
-        if (tid == 0) {
-            if (hdr_ok && a.bases[G - 1] + __ldcg(a.run_total + G - 1) != n_esc)
-                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            a.ctrl->op_gen[kOpDecompress] = sm.gen + 1;
+    // ---- the zero-point offset of run b: the sum of the earlier runs' totals ----
+    // Thread 0 waits until every run has published (one poller per CTA), then
+    // the CTA reads the totals it needs once; a flag not yet visible is polled.
+    bool waited = true;
+    if (tid == 0 && !wait_count(&a.ctrl->done[par], G)) sm.abort = 1;
+    __syncthreads();
+    uint64_t part = 0;
+    for (uint32_t r0 = tid; r0 < b && !sm.abort; r0 += 8 * kThreads) {
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t r = r0 + j * kThreads;
+            v[j] = r < b ? ld_relaxed_u64(flags + r) : kValid;
         }
-    });
-    if (!ok || !hdr_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (!entry_ready(v[j]) && waited) v[j] = poll_u64(flags + r0 + j * kThreads, entry_ready, &waited);
+            part += v[j] & ~kValid;
+        }
+    }
+    if (!waited) atomicExch(&sm.abort, 1u);
+    const uint64_t run_base = block_sum_u64<kThreads>(part, sm.scan64);
+    if (tid == 0 && b == G - 1 && run_base + run_total != sm.n_esc) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+    // publish my run's entries: flag | offset << 13 | count
+    for (uint32_t c = lo + tid; c < hi; c += kThreads) {
+        const uint32_t last0 = hi - 1 - (hi - 1 - lo) % kThreads;  // first chunk of the last batch
+        const uint64_t e = c >= last0 ? (sm.rloc[c - last0] << kCountBits) | sm.rcnt[c - last0]
+                                      : __ldcg(a.entry + c);
+        st_relaxed_u64(a.entry + c, kValid | (e + (run_base << kCountBits)));
+    }
+    __syncthreads();
+    if (sm.abort) {  // an earlier run's total never came (bounded wait ran out)
         if (tid == 0) {
-            if (!ok) report(a.status, ZCCL_ERR_TIMEOUT);
-            else if (b == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            report(a.status, ZCCL_ERR_TIMEOUT);
             for (int i = 0; i < 2; ++i) {  // let the started copies land
                 if (sm.chunk[i] >= T) continue;
                 mbar_arrive(&sm.bar[i]);
                 mbar_wait(&sm.bar[i], 0);
             }
+            call_end(a.ctrl, calls, sm.hdr_ok && published == G - 1);
         }
         return;
     }
     const uint32_t lut_lo = sm.lut_lo, lut_hi = sm.lut_hi;
-    uint32_t* tickets = &a.ctrl->ticket[kOpDecompress][sm.gen & 1];
 
     // ---- phase 2: stream chunks taken by ticket ----
+    uint32_t tn = T;  // thread 0: the next ticket, drawn one iteration ahead
+    uint64_t en = 0;  // thread 0: its entry, read one iteration ahead
     if (tid == 0) {
+        bool ok = true;
+        uint64_t e[2] = {0, 0};
         for (int i = 0; i < 2; ++i)
-            if (sm.chunk[i] < T) start_zp(a, sm, i, T, G);
+            if (sm.chunk[i] < T) e[i] = poll_u64(a.entry + sm.chunk[i], entry_ready, &ok);
+        if (!ok) {  // cannot happen unless a run never published: let the started copies land
+            report(a.status, ZCCL_ERR_TIMEOUT);
+            for (int i = 0; i < 2; ++i) {
+                if (sm.chunk[i] >= T) continue;
+                mbar_arrive(&sm.bar[i]);
+                mbar_wait(&sm.bar[i], 0);
+            }
+            sm.abort = 1;
+        } else {
+            for (int i = 0; i < 2; ++i)
+                if (sm.chunk[i] < T) start_zp(a, sm, i, sm.chunk[i], e[i]);
+            if (sm.chunk[1] < T) tn = atomicAdd(&a.ctrl->dticket[par], 1u);
+        }
     }
     __syncthreads();
+    if (sm.abort) {
+        if (tid == 0) call_end(a.ctrl, calls, sm.hdr_ok && published == G - 1);
+        return;
+    }
     for (uint32_t k = 0;; ++k) {
         const int buf = k & 1;
         const uint32_t c = sm.chunk[buf];
@@ -407,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             }
             break;
         }
+        if (tid == 0 && tn < T) en = ld_relaxed_u64(a.entry + tn);  // used at the refill below
         const uint8_t* blk = sm.blk[buf];
         uint32_t esc = 0;
         if (tid < (int)(L / 32)) {
@@ -449,15 +532,27 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
         }
         __syncthreads();  // buffer buf (block, zero-point run, expo) is free again
         if (tid == 0) {
-            const uint32_t t = atomicAdd(tickets, 1u);
+            uint32_t t = tn;
+            if (t < T && !entry_ready(en)) {  // its run had not published yet
+                bool ok = true;
+                en = poll_u64(a.entry + t, entry_ready, &ok);
+                if (!ok) {
+                    report(a.status, ZCCL_ERR_TIMEOUT);
+                    t = T;
+                }
+            }
             sm.chunk[buf] = t;
             if (t < T) {
                 start_block(a, sm, t, buf);
-                start_zp(a, sm, buf, T, G);
+                start_zp(a, sm, buf, t, en);
+                tn = atomicAdd(&a.ctrl->dticket[par], 1u);
+            } else {
+                tn = T;
             }
         }
         __syncthreads();
     }
+    if (tid == 0) call_end(a.ctrl, calls, sm.hdr_ok && published == G - 1);
 }
 
 template <typename K>

@@ -68,40 +68,34 @@ bool lut_ok(const zccl_lut_t* lut)
 
 uint64_t ranges_of(uint64_t units) { return (units + kRangeChunks - 1) / kRangeChunks; }
 
-// Every workspace starts with the same prefix: the control words, then the
-// compression run accumulators (two sets of kMaxGrid), which only
-// compression touches -- so a workspace can serve any op in any order.
-constexpr uint64_t kRunAccBytes = 2ull * 8 * kMaxGrid;
-constexpr uint64_t kPrefixBytes = kCtrlBytes + kRunAccBytes;
+// Every workspace starts with the same prefix (kPrefixBytes): the control
+// words, then the two parity sets of run flag words.  Each op leaves the
+// scratch after it all zero, so a workspace can serve any op in any order.
+static_assert(kFlagWords == kMaxGrid, "one flag word per CTA");
 
 // Compression workspace: prefix | escape count per chunk | a 4096-byte
 // escape staging slot per chunk.
 struct CompressLayout {
-    uint64_t run_acc, counts, stage, total;
+    uint64_t counts, stage, total;
 };
 CompressLayout compress_layout(uint64_t units)
 {
     CompressLayout l;
-    l.run_acc = kCtrlBytes;
     l.counts = kPrefixBytes;
     l.stage = round_up(l.counts + 4 * units, 256);
     l.total = round_up(l.stage + (uint64_t)kChunk * units, 256);
     return l;
 }
 
-// Decompression workspace: prefix | escapes per run | run base | chunk
-// offset within its run | escapes per chunk.
+// Decompression workspace: prefix | one entry word per chunk.
 struct DecompressLayout {
-    uint64_t run_total, bases, local, count, total;
+    uint64_t entry, total;
 };
 DecompressLayout decompress_layout(uint64_t units)
 {
     DecompressLayout l;
-    l.run_total = kPrefixBytes;
-    l.bases = l.run_total + 4ull * kMaxGrid;
-    l.local = l.bases + 8ull * kMaxGrid;
-    l.count = l.local + 4 * units;
-    l.total = round_up(l.count + 4 * units, 256);
+    l.entry = kPrefixBytes;
+    l.total = round_up(l.entry + 8 * units, 256);
     return l;
 }
 
@@ -208,7 +202,7 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.run_acc = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.run_acc);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -238,7 +232,7 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     std::memcpy(a.lut, lut->exp, 7);
     a.out_bytes = d_out_bytes;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.run_acc = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.run_acc);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
@@ -266,10 +260,8 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
     a.out = d_out;
     a.n = n;
     a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.run_total = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.run_total);
-    a.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
-    a.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
-    a.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.entry = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.entry);
     a.status = d_status;
     return launch_decompress(a, grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
@@ -307,6 +299,7 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
     a.S = S;
     a.out = d_out;
     a.n = n;
+    a.ctrl = sc.ctrl;
     a.bases = sc.bases;
     a.local = sc.local;
     a.count = sc.count;

@@ -12,7 +12,7 @@ namespace zccl {
 
 struct WsCtrl;
 
-// Compression, one stream or a batch of segments (blocks + placement kernels).
+// Compression, one stream or a batch of segments (one cooperative kernel).
 struct CompressArgs {
     const zccl_segment_t* segs;  // device descriptors (batched) or nullptr
     zccl_segment_t single;       // the one segment when segs == nullptr
@@ -21,7 +21,7 @@ struct CompressArgs {
     uint8_t lut[8];
     uint64_t* out_bytes;         // device [n_segs]
     WsCtrl* ctrl;
-    uint64_t* run_acc;           // [2][kMaxGrid] per-run escapes since the run's last segment start
+    uint64_t* flags;             // [2][kFlagWords] run flag words, by call parity
     uint32_t* counts;            // [max_units] escapes per chunk
     uint8_t* stage;              // [max_units * 4096] escapes, chunk-local
     uint32_t* status;
@@ -49,10 +49,8 @@ struct DecompressArgs {
     uint16_t* out;
     uint64_t n;
     WsCtrl* ctrl;
-    uint32_t* run_total;         // [grid] escapes of each CTA's run
-    uint64_t* bases;             // [grid] each run's offset into the zero-point array
-    uint32_t* local;             // [units] chunk offset within its run
-    uint32_t* count;             // [units] escapes per chunk
+    uint64_t* flags;             // [2][kFlagWords] run totals, by call parity
+    uint64_t* entry;             // [units] flag | zero-point offset << 13 | escapes
     uint32_t* status;
 };
 
@@ -62,9 +60,10 @@ struct ReduceArgs {
     uint32_t S;
     uint16_t* out;
     uint64_t n;
-    const uint64_t* bases;       // from the scan: [S][ranges per stream]
-    const uint32_t* local;       // [S][units]
-    const uint32_t* count;       // [S][units]
+    WsCtrl* ctrl;
+    uint64_t* bases;             // from the scan: [S][ranges per stream] (cleared by the last CTA)
+    uint32_t* local;             // [S][units] (each cleared once read)
+    uint32_t* count;             // [S][units] (each cleared once read)
     uint32_t* status;
 };
 

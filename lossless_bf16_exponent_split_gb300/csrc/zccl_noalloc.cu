@@ -66,8 +66,8 @@ extern "C" zccl_status_t zccl_decompress_noalloc(const void* d_in, uint64_t in_b
         return ZCCL_ERR_INVALID_ARG;
     void* ws = scratch_on_current_device();
     if (ws == nullptr) return ZCCL_ERR_CUDA;
-    // the arrival counters must start at zero; a call that stopped early
-    // (timeout) may have left them otherwise
-    if (cudaMemsetAsync(ws, 0, zccl::kCtrlBytes, stream) != cudaSuccess) return ZCCL_ERR_CUDA;
+    // the part of the workspace the call uses must start at zero; a call that
+    // stopped early (timeout) may have left it otherwise
+    if (cudaMemsetAsync(ws, 0, need, stream) != cudaSuccess) return ZCCL_ERR_CUDA;
     return zccl_decompress(d_in, in_bytes, d_out, n, ws, kNoAllocScratchBytes, d_status, stream);
 }

@@ -43,6 +43,7 @@ struct __align__(16) ReduceSmem {
     uint32_t zcount[kStages];
     uint32_t scan[kThreads / 32];
     uint32_t abort;
+    uint32_t last;
 };
 // followed by per-shard tables: const uint8_t* base[S]; uint64_t n_esc[S]; uint32_t lut[S][2]
 
@@ -97,43 +98,12 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
     if (zbytes) bulk_g2s(sm.zpb[st], t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
 }
 
-__global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
+// All threads of the CTA: the CTA's chunks (static stride), each over the S
+// shards in order.
+__device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
 {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    ReduceSmem& sm = *reinterpret_cast<ReduceSmem*>(smem_raw);
-    const ShardTables t = shard_tables(smem_raw, a.S);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t total = (uint32_t)units_of(a.n);
-
-    // every shard's header (the scan kernel reports a bad one; here it only
-    // stops this kernel from reading out of bounds)
-    bool ok = true;
-    for (uint32_t s = tid; s < a.S; s += kThreads) {
-        const uint8_t* base = reinterpret_cast<const uint8_t*>(a.streams[s]);
-        const uint64_t in_bytes = a.in_bytes[s];
-        bool good = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
-        if (good) {
-            const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
-            const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-            const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-            const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-            good = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
-                   zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
-            t.n_esc[s] = n_esc;
-            t.lut[2 * s] = h[6] << 8;
-            t.lut[2 * s + 1] = (h[6] >> 24) | (h[7] << 8);
-        }
-        t.base[s] = base;
-        ok = ok && good;
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
-        fence_mbar_init();
-        sm.abort = 0;
-    }
-    pdl_wait();  // offsets of the scan kernel
-    if (!__syncthreads_and(ok)) return;
-
     if (tid == 0)
         for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total);
 
@@ -204,6 +174,12 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
             }
         }
         if (s + 1 == a.S) {
+            // the chunk's offset words have had their one reader (issue_step,
+            // long done): clear them
+            for (uint32_t q = tid; q < a.S; q += kThreads) {
+                a.local[(uint64_t)q * total + c] = 0;
+                a.count[(uint64_t)q * total + c] = 0;
+            }
             uint16_t* dst = a.out + first;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -228,6 +204,58 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
         for (uint32_t jj = j + 1; jj < j + kStages; ++jj) {
             if (blockIdx.x + (jj / a.S) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
         }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    ReduceSmem& sm = *reinterpret_cast<ReduceSmem*>(smem_raw);
+    const ShardTables t = shard_tables(smem_raw, a.S);
+    const int tid = threadIdx.x;
+    const uint32_t total = (uint32_t)units_of(a.n);
+
+    // every shard's header (the scan kernel reports a bad one; here it only
+    // stops this kernel from reading out of bounds)
+    bool ok = true;
+    for (uint32_t s = tid; s < a.S; s += kThreads) {
+        const uint8_t* base = reinterpret_cast<const uint8_t*>(a.streams[s]);
+        const uint64_t in_bytes = a.in_bytes[s];
+        bool good = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
+        if (good) {
+            const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
+            const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+            const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
+            const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+            good = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
+                   zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
+            t.n_esc[s] = n_esc;
+            t.lut[2 * s] = h[6] << 8;
+            t.lut[2 * s + 1] = (h[6] >> 24) | (h[7] << 8);
+        }
+        t.base[s] = base;
+        ok = ok && good;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
+        fence_mbar_init();
+        sm.abort = 0;
+    }
+    pdl_wait();  // offsets of the scan kernel
+    if (__syncthreads_and(ok)) {
+        reduce_chunks(a, sm, t);
+    } else {  // a bad header: nothing to decode, but leave the scratch clear
+        for (uint32_t c = blockIdx.x; c < total; c += gridDim.x)
+            for (uint32_t s = tid; s < a.S; s += kThreads) {
+                a.local[(uint64_t)s * total + c] = 0;
+                a.count[(uint64_t)s * total + c] = 0;
+            }
+    }
+    // the last CTA to finish clears the range bases: the workspace is left
+    // all zero past its control block and flag area
+    if (arrive_last(a.ctrl, &sm.last)) {
+        const uint64_t nb = (uint64_t)a.S * ((total + kRangeChunks - 1) / kRangeChunks);
+        for (uint64_t i = tid; i < nb; i += kThreads) a.bases[i] = 0;
     }
 }
 

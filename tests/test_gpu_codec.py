@@ -186,3 +186,76 @@ def test_in_place_graph_of_calls_no_sync(codec):
     assert codec.read_status() == 0
     for x, out, nb in outs:
         assert stream_of(out, nb) == oracle.compress(x, lut)
+
+
+# Workspace bytes ahead of the per-call scratch: the control block (2048
+# bytes) and two call-parity sets of 4096 run flag words.
+WS_PREFIX = 2048 + 2 * 8 * 4096
+
+
+def _scratch_is_zero(codec) -> bool:
+    torch.cuda.synchronize()
+    ws = codec._ws
+    return bool((ws[WS_PREFIX:] == 0).all().item())
+
+
+def test_workspace_scratch_left_zero(codec):
+    """Every op leaves the workspace all zero past its control block and flag
+    sets (the decoder's per-chunk entry words rely on it when ops share a
+    workspace)."""
+    from lossless_bf16_exponent_split_gb300 import (OP_COMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS,
+                                                     OP_DECOMPRESS_REDUCE, zccl_workspace_bytes)
+    lut = LUTS["sigma1"]
+    x = workloads.activation_mix(rows=300, cols=4097, seed=3)  # ~4.5 % escapes, ragged tail
+    n = x.size
+    segs = [(0, 70_000), (70_000, 0), (70_000, 500_000), (570_000, n - 570_000)]
+    codec.workspace(max(zccl_workspace_bytes(OP_COMPRESS, n), zccl_workspace_bytes(OP_DECOMPRESS, n),
+                        zccl_workspace_bytes(OP_DECOMPRESS_REDUCE, n, 3),
+                        zccl_workspace_bytes(OP_COMPRESS_BATCHED, n, len(segs))))
+    want = oracle.compress(x, lut)
+    assert gpu_compress(codec, x, lut) == want
+    assert _scratch_is_zero(codec)
+    assert np.array_equal(gpu_decompress(codec, want, n), x)
+    assert _scratch_is_zero(codec)
+    codec.reset_status()
+    r = codec.decompress_reduce([dev_bytes(want)] * 3, [len(want)] * 3, n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    assert np.array_equal(host_u16(r), oracle.decompress_reduce([want] * 3, n))
+    assert _scratch_is_zero(codec)
+    xd = dev_u16(x)
+    pairs = []
+    for lo, cnt in segs:
+        pairs.append((xd[lo:lo + cnt], torch.empty(oracle.max_bytes(cnt), dtype=torch.uint8, device="cuda")))
+    codec.reset_status()
+    nb = codec.compress_batched(pairs, lut, total_n=n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    for (lo, cnt), (_, o), m in zip(segs, pairs, nb.cpu().tolist()):
+        assert o[:m].cpu().numpy().tobytes() == oracle.compress(x[lo:lo + cnt], lut)
+    assert _scratch_is_zero(codec)
+
+
+def test_long_runs_full_parity(codec):
+    """700M elements: each CTA's run of chunks spans more than one 128-chunk
+    batch in both kernels (grid <= 1216 CTAs), with a ragged tail; stream and
+    round trip bit-exact against the oracle."""
+    n = 700_000_000
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    xd = (torch.randn(n, device="cuda", generator=g) * 0.02).to(torch.bfloat16).view(torch.int16)
+    lut = LUTS["sigma0.02"]
+    codec.reset_status()
+    out, nb = codec.compress(xd, lut)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    m = int(nb.item())
+    x = xd.cpu().numpy().view(np.uint16)
+    want = oracle.compress(x, lut)
+    assert m == len(want)
+    assert out[:m].cpu().numpy().tobytes() == want
+    codec.reset_status()
+    y = codec.decompress(out, m, n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    assert torch.equal(y, xd)
