@@ -176,6 +176,12 @@ def max_over_ranks(pg, value: float, device):
     return float(t.item())
 
 
+def aggregate_gbs(world: int, step_bytes: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank processes step_bytes per step; the step
+    takes the slowest rank's time (weak scaling)."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 def barrier(pg, device=None):
     if pg is not None:
         if device is not None:
@@ -463,7 +469,7 @@ def main():
     kernel_ms = sum(k_ms.values())
     ms_per_step = kernel_ms if kind != "roundtrip" else region_ms / args.steps
     ms_per_step = max_over_ranks(pg, ms_per_step, dev)
-    value = world * step_input_bytes / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_gbs(world, step_input_bytes, ms_per_step)
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
