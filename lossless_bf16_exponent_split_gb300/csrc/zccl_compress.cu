@@ -228,15 +228,21 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
     return agg;
 }
 
-// Contiguous runs of the T chunks, one per CTA: run r = [run_lo(r), run_lo(r + 1)).
-__device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t G)
+// Runs: the T chunks cut into runs of 2^shift consecutive chunks, the
+// smallest power of two that leaves at most one run per CTA, so that a
+// chunk's run is a shift (no division on the per-chunk path).  CTA b takes
+// run b in phase 2; run r = [run_lo(r), run_lo(r + 1)).
+__device__ __forceinline__ uint32_t run_shift(uint32_t T, uint32_t G)
 {
-    return (uint32_t)(((uint64_t)r * T + G - 1) / G);
+    uint32_t sh = 0;
+    while (((uint64_t)T + (1ull << sh) - 1) >> sh > G) ++sh;
+    return sh;
 }
-__device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t T, uint32_t G)
+__device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t sh)
 {
-    return (uint32_t)((uint64_t)c * G / T);
+    return (uint32_t)min((uint64_t)r << sh, (uint64_t)T);
 }
+__device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t sh) { return c >> sh; }
 
 // A run's flag word: chunks of the run coded so far << 40 | the escapes of
 // those chunks that carry into the next run.
@@ -265,6 +271,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     const uint64_t total64 = segment_table(a, ustart, sm.scan64);  // (contains barriers)
     const bool fits = total64 <= a.max_units;
     const uint32_t T = fits ? (uint32_t)total64 : 0u;
+    const uint32_t sh = run_shift(T, G);
 
     // ---- phase 1: code chunks taken by ticket, stage escapes, count ----
     if (tid == 0) {
@@ -306,8 +313,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             a.counts[c] = agg;
             // the chunk's escapes carry into the next run unless its segment
             // ends inside this run
-            const uint32_t r = run_of(c, T, G);
-            const uint32_t carry = ustart[s + 1] >= run_lo(r + 1, T, G) ? agg : 0u;
+            const uint32_t r = run_of(c, sh);
+            const uint32_t carry = ustart[s + 1] >= run_lo(r + 1, T, sh) ? agg : 0u;
             uint64_t* acc = a.flags + (uint64_t)(calls & 1) * kFlagWords;
             atomicAdd((unsigned long long*)&acc[r], kDoneOne | carry);
             ++coded;
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             if (lane == 0) a.out_bytes[s] = kHeaderBytes;
         }
     }
-    const uint32_t lo = run_lo(b, T, G), hi = run_lo(b + 1, T, G);
+    const uint32_t lo = run_lo(b, T, sh), hi = run_lo(b + 1, T, sh);
     if (lo >= hi || sm.abort) {
         if (tid == 0) {
             bulk_wait0();
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         return;
     }
     const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
-    const uint32_t h0 = st < lo ? run_of(st, T, G) : b;  // flag words [h0, b) make the carry
+    const uint32_t h0 = st < lo ? run_of(st, sh) : b;  // flag words [h0, b) make the carry
     uint64_t part = 0;
     for (uint32_t q0 = h0 + tid; q0 < b; q0 += 8 * kThreads) {  // all loads of a round in flight at once
         uint64_t v[8];
