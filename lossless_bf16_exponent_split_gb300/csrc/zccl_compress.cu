@@ -92,6 +92,7 @@ struct __align__(16) CompressSmem {
     uint64_t off[kBatch];
     uint32_t abort;
     uint32_t par;
+    uint32_t calls;
     uint32_t next[2];  // the chunk of iteration k + 1, in next[(k + 1) & 1]: slow threads
                        // still read one slot while thread 0 fills the other
 };
@@ -246,6 +247,7 @@ __device__ __forceinline__ uint32_t run_of(uint32_t c, uint32_t sh) { return c >
 
 // A run's flag word: chunks of the run coded so far << 40 | the escapes of
 // those chunks that carry into the next run.
+constexpr int kBookkeeper = 32;  // lane 0 of warp 1: per-chunk counts and flag words
 constexpr uint32_t kDoneShift = 40;
 constexpr uint64_t kDoneOne = 1ull << kDoneShift;
 
@@ -258,8 +260,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     const uint32_t b = blockIdx.x, G = gridDim.x;
 
     uint32_t calls = 0;    // thread 0: read now, used once the first chunk is coded
-    uint32_t coded = 0;    // thread 0: chunks this CTA coded
-    bool last = false;     // thread 0: this CTA completed the call's done count
+    uint32_t coded = 0;    // bookkeeper: chunks this CTA coded
+    bool last = false;     // bookkeeper: this CTA completed the call's done count
     if (tid == 0) calls = call_read(a.ctrl);
     for (int e = tid; e < 256; e += kThreads) {
         uint32_t c = 0;
@@ -291,6 +293,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             const uint32_t tn = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
             sm.next[(k + 1) & 1] = tn;
             if (tn < T) issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
+            if (k == 0) sm.calls = calls;  // for the bookkeeper, after the first chunk
         }
         const uint32_t s = find_segment(ustart, a.n_segs, c);
         const zccl_segment_t d = seg_get(a, s);
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         const uint64_t first = (uint64_t)cl * kChunk;
         const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
         if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
+        if (tid == 0) bulk_wait_read0();  // the previous block's store has read the block buffer
         if (valid < kChunk) {  // tail: the last < 8 elements come by plain loads
             const uint32_t done = valid & ~7u;
             if (tid < (int)(valid - done))
@@ -309,16 +313,15 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             break;
         }
         const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid);
-        if (tid == 0) {
+        if (tid == kBookkeeper) {  // (thread 0 is busy with the tickets and the bulk copies)
             a.counts[c] = agg;
             // the chunk's escapes carry into the next run unless its segment
             // ends inside this run
             const uint32_t r = run_of(c, sh);
             const uint32_t carry = ustart[s + 1] >= run_lo(r + 1, T, sh) ? agg : 0u;
-            uint64_t* acc = a.flags + (uint64_t)(calls & 1) * kFlagWords;
+            uint64_t* acc = a.flags + (uint64_t)(sm.calls & 1) * kFlagWords;
             atomicAdd((unsigned long long*)&acc[r], kDoneOne | carry);
             ++coded;
-            bulk_wait_read0();
         }
         __syncthreads();
         c = sm.next[(k + 1) & 1];
@@ -329,10 +332,13 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     // Count this CTA's chunks (and the CTA itself) done: thread 0's release
     // add, after a barrier, orders everything the CTA wrote before it (its
     // counts, staged escapes and flag-word adds) ahead of the count.
-    if (tid == 0) sm.par = calls & 1;
+    if (tid == 0) {
+        sm.calls = calls;
+        sm.par = calls & 1;
+    }
     __syncthreads();
     const uint32_t par = sm.par;
-    if (tid == 0) last = atom_add_release_u32(&a.ctrl->done[par], coded + 1) + coded + 1 == T + G;
+    if (tid == kBookkeeper) last = atom_add_release_u32(&a.ctrl->done[par], coded + 1) + coded + 1 == T + G;
     clear_other_parity(a.ctrl, a.flags, par);
     const uint64_t* acc = a.flags + (uint64_t)par * kFlagWords;
 
@@ -347,10 +353,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     }
     if (!fits) {
         if (b == 0 && tid == 0) report(a.status, ZCCL_ERR_INVALID_ARG);
-        if (tid == 0) {
-            bulk_wait0();
-            call_end(a.ctrl, calls, last);
-        }
+        if (tid == 0) bulk_wait0();
+        if (tid == kBookkeeper) call_end(a.ctrl, sm.calls, last);
         return;
     }
     // empty, valid segments: header only (CTA 0)
@@ -364,10 +368,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     }
     const uint32_t lo = run_lo(b, T, sh), hi = run_lo(b + 1, T, sh);
     if (lo >= hi || sm.abort) {
-        if (tid == 0) {
-            bulk_wait0();
-            call_end(a.ctrl, calls, last);
-        }
+        if (tid == 0) bulk_wait0();
+        if (tid == kBookkeeper) call_end(a.ctrl, sm.calls, last);
         return;
     }
 
@@ -384,8 +386,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         if (tid == 0) {
             report(a.status, ZCCL_ERR_TIMEOUT);
             bulk_wait0();
-            call_end(a.ctrl, calls, last);
         }
+        if (tid == kBookkeeper) call_end(a.ctrl, sm.calls, last);
         return;
     }
     const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
@@ -466,10 +468,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         carry = carry_out;
         __syncthreads();
     }
-    if (tid == 0) {
-        bulk_wait0();  // the chunk blocks' bulk stores are written
-        call_end(a.ctrl, calls, last);
-    }
+    if (tid == 0) bulk_wait0();  // the chunk blocks' bulk stores are written
+    if (tid == kBookkeeper) call_end(a.ctrl, sm.calls, last);
 }
 
 }  // namespace
