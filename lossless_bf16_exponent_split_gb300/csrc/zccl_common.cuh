@@ -279,7 +279,9 @@ __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v)
 // Exclusive scan of `v` over a block of kThreads threads; returns the
 // exclusive prefix and writes the block total to *total.  `scratch` holds at
 // least kThreads/32 words.  Contains __syncthreads (call from all threads).
-template <int kThreads, typename T = uint32_t>
+// kTrailingBarrier = false skips the final barrier: only for callers that
+// pass another barrier before the scratch is written again.
+template <int kThreads, typename T = uint32_t, bool kTrailingBarrier = true>
 __device__ __forceinline__ T block_exclusive_scan(T v, T* scratch, T* total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -299,7 +301,7 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* scratch, T* total)
         all += t;
     }
     *total = all;
-    __syncthreads();  // scratch may be reused right after
+    if (kTrailingBarrier) __syncthreads();  // scratch may be reused right after
     return before + incl - v;
 }
 

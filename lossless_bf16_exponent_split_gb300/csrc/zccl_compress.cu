@@ -15,7 +15,8 @@
 // contiguous run per CTA for the scan.  No CTA ever waits for the whole grid.
 //
 //  Phase 1 streams the input once.  CTAs take chunks by atomic ticket (SMs
-//    that get their data faster take more chunks).  Each chunk's 8 KB arrives
+//    that get their data faster take more chunks; each ticket is drawn one
+//    chunk before it is needed).  Each chunk's 8 KB arrives
 //    in shared memory by a TMA bulk copy, double-buffered so the next chunk
 //    lands while this one is coded.  A thread codes 8 consecutive elements
 //    from one 16-byte shared load: byte permutes give the sign-mantissa
@@ -217,7 +218,7 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
         esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
     }
     uint32_t agg;
-    const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+    const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
     uint8_t* dst = a.stage + (uint64_t)c * kChunk + excl;
     const uint16_t* x16 = reinterpret_cast<const uint16_t*>(src);
     uint32_t m = esc, j = 0;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     uint32_t coded = 0;    // bookkeeper: chunks this CTA coded
     bool last = false;     // bookkeeper: this CTA completed the call's done count
     if (tid == 0) calls = call_read(a.ctrl);
+    uint32_t tn_pf = 0xFFFFFFFFu;  // thread 0: the ticket after next, drawn one chunk ahead
     for (int e = tid; e < 256; e += kThreads) {
         uint32_t c = 0;
 #pragma unroll
@@ -283,16 +285,22 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         sm.abort = 0;
         const uint32_t t = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
         sm.next[0] = t;
-        if (t < T) issue_chunk_load(a, ustart, sm, t, 0);
+        if (t < T) {
+            issue_chunk_load(a, ustart, sm, t, 0);
+            tn_pf = draw_ticket(a.ctrl);
+        }
     }
     __syncthreads();
     uint32_t c = sm.next[0], k = 0;
     while (c < T) {
         const int buf = k & 1;
         if (tid == 0) {  // the next chunk (the load of this one is in flight)
-            const uint32_t tn = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
+            const uint32_t tn = consume_ticket(a.ctrl, tn_pf, T);
             sm.next[(k + 1) & 1] = tn;
-            if (tn < T) issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
+            if (tn < T) {
+                issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
+                tn_pf = draw_ticket(a.ctrl);
+            }
             if (k == 0) sm.calls = calls;  // for the bookkeeper, after the first chunk
         }
         const uint32_t s = find_segment(ustart, a.n_segs, c);

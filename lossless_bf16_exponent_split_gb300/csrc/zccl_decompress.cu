@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
         }
         uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+        const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
         const bool good = agg == sm.zcount[buf];
         if (good) {
             const uint8_t* src = sm.zpb[buf] + sm.zdelta[buf] + excl;

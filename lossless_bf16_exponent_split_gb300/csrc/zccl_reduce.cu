@@ -137,7 +137,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
         }
         uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads>((uint32_t)__popc(esc), sm.scan, &agg);
+        const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
         if (agg == sm.zcount[st]) {
             const uint8_t* src = sm.zpb[st] + sm.zdelta[st] + excl;
             uint32_t m = esc, jj = 0;
