@@ -52,6 +52,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr uint32_t kInBytes = kChunk * 2;  // 8192
 constexpr uint32_t kBatch = kThreads;       // chunks placed per round in phase 2
+constexpr uint32_t kAborted = 0xFFFFFFFFu;  // code_chunk: the chunk's load never landed
 
 __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
 
@@ -162,7 +163,8 @@ __device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t 
 // Codes one chunk (already in sm.in[buf]) into sm.blk, stores the block and
 // stages the escapes; returns the chunk's escape count (all threads).
 __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSmem& sm, int buf, uint32_t c,
-                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid)
+                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid,
+                                               bool timed_out)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t L = slots_of(valid);
@@ -204,7 +206,9 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
         planes[L / 4] = (uint8_t)(acc >> 16);
     }
     fence_proxy_async_smem();
-    __syncthreads();
+    // (also the CTA's verdict on the chunk's load: if it never landed in
+    // some thread's bounded wait, nothing is stored)
+    if (__syncthreads_or(timed_out)) return kAborted;
     if (tid == 0) {
         bulk_s2g((uint8_t*)d.out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
         bulk_commit();
@@ -308,19 +312,22 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         const uint32_t cl = c - ustart[s];
         const uint64_t first = (uint64_t)cl * kChunk;
         const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
-        if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
-        if (tid == 0) bulk_wait_read0();  // the previous block's store has read the block buffer
+        const bool timed_out = !mbar_wait(&sm.bar[buf], (k >> 1) & 1);
         if (valid < kChunk) {  // tail: the last < 8 elements come by plain loads
             const uint32_t done = valid & ~7u;
-            if (tid < (int)(valid - done))
+            if (tid < (int)(valid - done) && !timed_out)
                 reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
+            __syncthreads();
         }
-        __syncthreads();
-        if (sm.abort) {  // a bulk load never landed (bounded wait ran out)
-            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
+        const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid, timed_out);
+        if (agg == kAborted) {  // a bulk load never landed (bounded wait ran out)
+            if (tid == 0) {
+                sm.abort = 1;
+                report(a.status, ZCCL_ERR_TIMEOUT);
+            }
+            __syncthreads();
             break;
         }
-        const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid);
         if (tid == kBookkeeper) {  // (thread 0 is busy with the tickets and the bulk copies)
             a.counts[c] = agg;
             // the chunk's escapes carry into the next run unless its segment
@@ -331,6 +338,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             atomicAdd((unsigned long long*)&acc[r], kDoneOne | carry);
             ++coded;
         }
+        if (tid == 0) bulk_wait_read0();  // the block's store has read the block buffer
         __syncthreads();
         c = sm.next[(k + 1) & 1];
         ++k;
