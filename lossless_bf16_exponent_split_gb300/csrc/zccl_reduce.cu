@@ -63,22 +63,41 @@ __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t 
     return t;
 }
 
+// Offsets of one step's zero-point run: the range base plus the chunk's
+// prefix within its range, and its escape count (loaded one iteration ahead
+// of their use by issue_step, so thread 0 never waits on them).
+struct StepOffsets {
+    uint64_t base;
+    uint32_t local, count;
+};
+
+__device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t j, uint32_t total)
+{
+    StepOffsets o{0, 0, 0};
+    const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
+    if (c >= total) return o;
+    const uint32_t s = j % a.S;
+    const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
+    const uint64_t idx = (uint64_t)s * total + c;
+    o.base = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks);
+    o.local = __ldcg(a.local + idx);
+    o.count = __ldcg(a.count + idx);
+    return o;
+}
+
 // Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / S) * gridDim.x,
 // shard j % S) into stage j % kStages.
 __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t j,
-                                           uint32_t total)
+                                           uint32_t total, const StepOffsets& off)
 {
     const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
     if (c >= total) return;
     const uint32_t s = j % a.S;
     const int st = j % kStages;
-    const uint32_t units = total;
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;
-    const uint64_t idx = (uint64_t)s * units + c;
-    const uint64_t o0 = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks) + __ldcg(a.local + idx);
-    const uint64_t o1 = o0 + __ldcg(a.count + idx);
+    const uint64_t o0 = off.base + off.local;
+    const uint64_t o1 = o0 + off.count;
     uint32_t zbytes = 0, delta = 0, cnt = 0;
     const uint64_t zp = zp_offset_of(a.n);
     if (o1 <= t.n_esc[s] && o1 - o0 <= kChunk) {
@@ -99,25 +118,30 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
 }
 
 // All threads of the CTA: the CTA's chunks (static stride), each over the S
-// shards in order.
+// shards in order.  The fp32 sums are kept as pairs and added with the
+// two-lane add (each lane rounds to nearest even exactly as a scalar add).
 __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t total = (uint32_t)units_of(a.n);
-    if (tid == 0)
-        for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total);
+    StepOffsets ahead{0, 0, 0};  // thread 0: offsets of the next step to queue
+    if (tid == 0) {
+        for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total, load_offsets(a, j, total));
+        ahead = load_offsets(a, kStages - 1, total);
+    }
 
-    float acc[32];
+    float2 acc[16];
 #pragma unroll
-    for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
+    for (int q = 0; q < 16; ++q) acc[q] = make_float2(0.0f, 0.0f);
 
-    uint32_t j = 0;
+    uint32_t j = 0, s = 0, c = blockIdx.x;  // step, its shard and its chunk
     for (;; ++j) {
-        const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
         if (c >= total) break;
-        const uint32_t s = j % a.S;
         const int st = j % kStages;
-        if (tid == 0) issue_step(a, sm, t, j + kStages - 1, total);
+        if (tid == 0) {
+            issue_step(a, sm, t, j + kStages - 1, total, ahead);
+            ahead = load_offsets(a, j + kStages, total);
+        }
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
@@ -161,21 +185,14 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
                 const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const float f0 = __uint_as_float(w[q] << 16);
-                    const float f1 = __uint_as_float(w[q] & 0xFFFF0000u);
-                    if (s == 0) {
-                        acc[8 * i + 2 * q] = f0;
-                        acc[8 * i + 2 * q + 1] = f1;
-                    } else {
-                        acc[8 * i + 2 * q] = __fadd_rn(acc[8 * i + 2 * q], f0);
-                        acc[8 * i + 2 * q + 1] = __fadd_rn(acc[8 * i + 2 * q + 1], f1);
-                    }
+                    const float2 f = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
+                    acc[4 * i + q] = s == 0 ? f : __fadd2_rn(acc[4 * i + q], f);
                 }
             }
         }
         if (s + 1 == a.S) {
-            // the chunk's offset words have had their one reader (issue_step,
-            // long done): clear them
+            // the chunk's offset words have had their one reader (loaded
+            // steps ago): clear them
             for (uint32_t q = tid; q < a.S; q += kThreads) {
                 a.local[(uint64_t)q * total + c] = 0;
                 a.count[(uint64_t)q * total + c] = 0;
@@ -186,10 +203,10 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
                 const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
                 if (e0 >= valid) continue;
                 uint4 o;
-                o.x = rne_bf16(acc[8 * i + 0]) | (rne_bf16(acc[8 * i + 1]) << 16);
-                o.y = rne_bf16(acc[8 * i + 2]) | (rne_bf16(acc[8 * i + 3]) << 16);
-                o.z = rne_bf16(acc[8 * i + 4]) | (rne_bf16(acc[8 * i + 5]) << 16);
-                o.w = rne_bf16(acc[8 * i + 6]) | (rne_bf16(acc[8 * i + 7]) << 16);
+                o.x = rne_bf16(acc[4 * i + 0].x) | (rne_bf16(acc[4 * i + 0].y) << 16);
+                o.y = rne_bf16(acc[4 * i + 1].x) | (rne_bf16(acc[4 * i + 1].y) << 16);
+                o.z = rne_bf16(acc[4 * i + 2].x) | (rne_bf16(acc[4 * i + 2].y) << 16);
+                o.w = rne_bf16(acc[4 * i + 3].x) | (rne_bf16(acc[4 * i + 3].y) << 16);
                 if (e0 + 8 <= valid) {
                     *reinterpret_cast<uint4*>(dst + e0) = o;
                 } else {
@@ -198,6 +215,10 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             }
         }
         __syncthreads();
+        if (++s == a.S) {  // next step: the next shard, or the next chunk's first
+            s = 0;
+            c += gridDim.x;
+        }
     }
     // steps still in flight after an early stop: wait for them (bounded)
     if (tid == 0 && sm.abort) {
