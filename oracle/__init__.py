@@ -67,6 +67,8 @@ def _load():
             "zo_decompress": ([u8p, ctypes.c_uint64, u16p, ctypes.c_uint64], ctypes.c_int),
             "zo_decompress_reduce": ([ctypes.POINTER(u8p), u64p, ctypes.c_uint32, u16p,
                                       ctypes.c_uint64], ctypes.c_int),
+            "zo_decompress_reduce_local": ([ctypes.POINTER(u8p), u64p, ctypes.c_uint32, u16p, ctypes.c_uint32,
+                                            ctypes.c_int, u16p, ctypes.c_uint64], ctypes.c_int),
             "zo_round_bf16": ([ctypes.c_float], ctypes.c_uint16),
             "zo_round_bf16_n": ([ctypes.POINTER(ctypes.c_float), u16p, ctypes.c_uint64], None),
         }
@@ -163,6 +165,33 @@ def decompress_reduce(streams, n: int) -> np.ndarray:
                                       _ptr(out, ctypes.c_uint16), n)
     if st != OK:
         raise OracleError(st, "decompress_reduce")
+    return out[:n]
+
+
+def decompress_reduce_local(streams, n: int, local=None, local_pos: int = 0, initial=None) -> np.ndarray:
+    """ZipCCL 2.D local reduction as one rank sees it: `streams` in rank
+    order, where position local_pos is the rank's own uncompressed BF16
+    shard `local` (its entry in `streams` is ignored); with `initial` (BF16
+    bits) the fold starts from those values (accumulate into an existing
+    output)."""
+    S = len(streams)
+    bufs = [np.frombuffer(bytes(s if s is not None else b"\0"), np.uint8).copy() for s in streams]
+    ptrs = (ctypes.POINTER(ctypes.c_uint8) * S)(*[_ptr(b, ctypes.c_uint8) for b in bufs])
+    sizes = np.array([b.size for b in bufs], np.uint64)
+    out = np.zeros(max(n, 1), np.uint16)
+    if initial is not None:
+        out[:n] = np.asarray(initial, np.uint16)[:n]
+    loc = None
+    if local is not None:
+        loc = np.ascontiguousarray(np.asarray(local, np.uint16)[:n])
+        if loc.size == 0:
+            loc = np.zeros(1, np.uint16)
+    st = _load().zo_decompress_reduce_local(ptrs, _ptr(sizes, ctypes.c_uint64), S,
+                                            _ptr(loc, ctypes.c_uint16) if loc is not None else None,
+                                            local_pos, 1 if initial is not None else 0,
+                                            _ptr(out, ctypes.c_uint16), n)
+    if st != OK:
+        raise OracleError(st, "decompress_reduce_local")
     return out[:n]
 
 

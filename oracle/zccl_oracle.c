@@ -355,3 +355,47 @@ int zo_decompress_reduce(const uint8_t* const* in, const uint64_t* in_bytes, uin
     free(dec);
     return st;
 }
+
+/* The local-reduction step as a rank of a zipped reduce-scatter sees it
+ * (ZipCCL 2.D): S inputs in rank order, every one a compressed stream except
+ * the rank's own shard at position local_pos, which is plain BF16 (local may
+ * be NULL: then all S are streams and local_pos is ignored).  With
+ * accumulate != 0 the fold starts from the BF16 values already in out:
+ *   acc = accumulate ? out[i] : x_0;  acc += x_s for the remaining inputs in
+ *   order;  out[i] = round_bf16(acc)
+ * in float, one IEEE add at a time [R14].  in[local_pos] is not read. */
+int zo_decompress_reduce_local(const uint8_t* const* in, const uint64_t* in_bytes, uint32_t S,
+                               const uint16_t* local, uint32_t local_pos, int accumulate,
+                               uint16_t* out, uint64_t n)
+{
+    if (in == NULL || in_bytes == NULL || S == 0 || (n > 0 && out == NULL)) return ZO_INVALID_ARG;
+    if (local != NULL && local_pos >= S) return ZO_INVALID_ARG;
+    uint16_t** dec = calloc(S, sizeof(uint16_t*));
+    if (!dec) return ZO_INVALID_ARG;
+    int st = ZO_OK;
+    for (uint32_t s = 0; s < S && st == ZO_OK; s++) {
+        if (local != NULL && s == local_pos) continue;
+        dec[s] = malloc((n ? n : 1) * sizeof(uint16_t));
+        if (!dec[s]) { st = ZO_INVALID_ARG; break; }
+        st = zo_decompress(in[s], in_bytes[s], dec[s], n);
+    }
+    if (st == ZO_OK) {
+        for (uint64_t i = 0; i < n; i++) {
+            float acc = 0.0f;
+            int have = 0;
+            if (accumulate) {
+                acc = bf16_to_float(out[i]);
+                have = 1;
+            }
+            for (uint32_t s = 0; s < S; s++) {
+                const uint16_t v = (local != NULL && s == local_pos) ? local[i] : dec[s][i];
+                acc = have ? acc + bf16_to_float(v) : bf16_to_float(v);
+                have = 1;
+            }
+            out[i] = zo_round_bf16(acc);
+        }
+    }
+    for (uint32_t s = 0; s < S; s++) free(dec[s]);
+    free(dec);
+    return st;
+}

@@ -116,3 +116,51 @@ def test_reduce_rejects_mismatched_n():
     with pytest.raises(oracle.OracleError) as e:
         oracle.decompress_reduce([s1, s2], 100)
     assert e.value.status == oracle.CORRUPT
+
+
+def _numpy_fold(parts):
+    """In-order float32 left fold of BF16 bit arrays, rounded by torch's
+    cast (NaN -> 0x7FC0): the definition the oracle must meet."""
+    with np.errstate(all="ignore"):
+        acc = bits_to_f32(parts[0])
+        for x in parts[1:]:
+            acc = (acc + bits_to_f32(x)).astype(np.float32)
+    want = torch_bf16_bits(acc).copy()
+    want[np.isnan(acc)] = 0x7FC0
+    return want
+
+
+@pytest.mark.parametrize("local_pos", [0, 2, 4])
+def test_reduce_local_shard_at_each_position(local_pos):
+    """ZipCCL 2.D from one rank's view: the rank's own shard enters the fold
+    uncompressed, at its rank position."""
+    n = 2 * 4096 + 301
+    S = 5
+    shards = [workloads.special_values(n, seed=10 + s, frac=0.05) for s in range(S)]
+    lut = oracle.lut_from_sigma(1.0)
+    streams = [None if s == local_pos else oracle.compress(x, lut) for s, x in enumerate(shards)]
+    got = oracle.decompress_reduce_local(streams, n, local=shards[local_pos], local_pos=local_pos)
+    assert np.array_equal(got, _numpy_fold(shards))
+
+
+def test_reduce_accumulates_into_existing_output():
+    n = 4096 + 9
+    S = 3
+    shards = [workloads.special_values(n, seed=30 + s, frac=0.05) for s in range(S)]
+    initial = workloads.special_values(n, seed=99, frac=0.05)
+    lut = oracle.lut_from_sigma(1.0)
+    streams = [oracle.compress(x, lut) for x in shards]
+    got = oracle.decompress_reduce_local(streams, n, initial=initial)
+    assert np.array_equal(got, _numpy_fold([initial] + shards))
+    # both at once: the existing output first, then the shards with the local one in place
+    streams[1] = None
+    got = oracle.decompress_reduce_local(streams, n, local=shards[1], local_pos=1, initial=initial)
+    assert np.array_equal(got, _numpy_fold([initial] + shards))
+
+
+def test_reduce_single_local_shard_is_canonical_copy():
+    x = workloads.special_values(5000, seed=7, frac=0.3)
+    got = oracle.decompress_reduce_local([None], x.size, local=x, local_pos=0)
+    want = x.copy()
+    want[((x & 0x7F80) == 0x7F80) & ((x & 0x7F) != 0)] = 0x7FC0  # every NaN becomes the canonical one
+    assert np.array_equal(got, want)
