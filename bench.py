@@ -9,7 +9,8 @@ L2-resident, as it would not be after crossing the network).  Three rotating
 buffer sets, 316 MB touched per step (> 129 MB L2), keep every step's inputs
 out of L2.  Other workloads (--workload): activation_mix (compress +
 decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
-rs_local (decompress-reduce of 8 shards), gauss1m.
+rs_local (decompress-reduce of 8 shards), rs_local_own (the same with the rank's own shard
+uncompressed), gauss1m.
 
 Prints ONE JSON line (rank 0).  `value` = GB/s of BF16 input through the step
 (2n bytes per compress and per decompress; reduce: 2 S n), whole job.
@@ -42,7 +43,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="zccl", choices=["zccl", "reference"])
     p.add_argument("--workload", default="llama3_8b_allgather",
-                   choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "gauss1m"])
+                   choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "rs_local_own",
+                            "gauss1m"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -208,8 +210,9 @@ def make_inputs(name, seed):
         m = w.moe_payload(tokens=cfg["tokens"], top_k=cfg["top_k"], experts=cfg["experts"],
                           hidden=cfg["hidden"], seed=seed)
         return "batched", m.payload, cfg["sigma"], m
-    if name == "rs_local":
-        return "reduce", w.reduce_shards(cfg["S"], cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"], None
+    if name in ("rs_local", "rs_local_own"):
+        return ("reduce", w.reduce_shards(cfg["S"], cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"],
+                cfg.get("local_pos"))
     raise ValueError(name)
 
 
@@ -220,14 +223,18 @@ def cpu_baseline(name, budget_s=12.0):
     cfg = w.CONFIGS[name]
     sigma = cfg["sigma"]
     lut = oracle.lut_from_sigma(sigma)
-    if name == "rs_local":
+    if name in ("rs_local", "rs_local_own"):
         n = 1 << 21
         shards = w.reduce_shards(cfg["S"], n, sigma, seed=0)
-        streams = [oracle.compress(x, lut) for x in shards]
+        lp = cfg.get("local_pos")
+        streams = [None if s == lp else oracle.compress(x, lut) for s, x in enumerate(shards)]
         t0 = time.perf_counter()
         reps = 0
         while True:
-            oracle.decompress_reduce(streams, n)
+            if lp is None:
+                oracle.decompress_reduce(streams, n)
+            else:
+                oracle.decompress_reduce_local(streams, n, local=shards[lp], local_pos=lp)
             reps += 1
             if time.perf_counter() - t0 > budget_s / 2:
                 break
@@ -263,11 +270,15 @@ def run_reference(args):
     cfg = w.CONFIGS[cfg_name]
     lut = oracle.lut_from_sigma(cfg["sigma"])
     # each step: a bounded sample of the workload (oracle speed ~0.1-0.3 GB/s)
-    if cfg_name == "rs_local":
+    if cfg_name in ("rs_local", "rs_local_own"):
         n = 1 << 20
         shards = w.reduce_shards(cfg["S"], n, cfg["sigma"], seed=0)
-        streams = [oracle.compress(x, lut) for x in shards]
-        step = lambda: oracle.decompress_reduce(streams, n)
+        lp = cfg.get("local_pos")
+        streams = [None if s == lp else oracle.compress(x, lut) for s, x in enumerate(shards)]
+        if lp is None:
+            step = lambda: oracle.decompress_reduce(streams, n)
+        else:
+            step = lambda: oracle.decompress_reduce_local(streams, n, local=shards[lp], local_pos=lp)
         unit_bytes = 2 * cfg["S"] * n
         sample = f"decompress_reduce of {cfg['S']} shards x {n} elements per step"
     else:
@@ -402,30 +413,41 @@ def main():
         cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
                      "step": "one batched compress of all static+dynamic segments",
                      "l2": "input 537 MB > 129 MB L2"}
-    else:  # reduce
+    else:  # reduce (with the rank's own shard uncompressed at local_pos, if given)
         shards = host
+        local_pos = extra
         S = len(shards)
         n = shards[0].size
         codec = z.Codec(dev)
         streams, sizes = [], []
-        for x in shards:
+        for s_, x in enumerate(shards):
+            if s_ == local_pos:
+                streams.append(None)
+                sizes.append(None)
+                continue
             o, nbt = codec.compress(tdev(x), lut)
             streams.append(o)
             sizes.append(nbt)
         torch.cuda.synchronize()
-        sizes_h = [int(s.item()) for s in sizes]
-        ptrs = torch.tensor([s.data_ptr() for s in streams], dtype=torch.int64, device=dev)
+        sizes_h = [0 if v is None else int(v.item()) for v in sizes]
+        ptrs = torch.tensor([0 if o is None else o.data_ptr() for o in streams], dtype=torch.int64, device=dev)
         inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
+        local = tdev(shards[local_pos]) if local_pos is not None else None
         y = torch.empty(n, dtype=torch.int16, device=dev)
         wsb = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, n, S)
         ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
         def red():
-            z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n, ws.data_ptr(),
-                                             wsb, st_ptr, h), "decompress_reduce")
+            if local is None:
+                z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n,
+                                                 ws.data_ptr(), wsb, st_ptr, h), "decompress_reduce")
+            else:
+                z.check(z.zccl_decompress_reduce_local(ptrs.data_ptr(), inb.data_ptr(), S, local.data_ptr(),
+                                                       local_pos, 0, y.data_ptr(), n, ws.data_ptr(), wsb, st_ptr,
+                                                       h), "decompress_reduce_local")
         names = ["decompress_reduce"]
-        alg = {"decompress_reduce": sum(sizes_h) + 2 * n}
+        alg = {"decompress_reduce": sum(sizes_h) + (2 * n if local is not None else 0) + 2 * n}
         step_input_bytes = 2 * S * n
 
         def step(k, ev=None):
@@ -437,7 +459,8 @@ def main():
                 ev[1].record(stream)
                 ev[2].record(stream)
         cfg_extra = {"n": n, "shards": S, "stream_bytes_total": sum(sizes_h),
-                     "step": "one fused decompress+reduce of S shards",
+                     "step": "one fused decompress+reduce of S shards"
+                             + (f" (shard {local_pos} uncompressed)" if local is not None else ""),
                      "l2": "512 MB write between steps flushes L2 (outside kernel events)"}
 
     # ---- warm-up, then K timed steps ----

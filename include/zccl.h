@@ -170,6 +170,23 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
                                      uint64_t ws_bytes, uint32_t* d_status,
                                      cudaStream_t stream);
 
+/* The same local reduction as one rank of a zipped reduce-scatter runs it
+ * (ZipCCL 2.D): the S inputs in rank order are the other ranks' compressed
+ * streams plus the rank's own shard, which it holds uncompressed.
+ *   d_local:    that shard, n plain BF16 values in device memory (16-byte
+ *               aligned), at position local_pos (< S) of the fold; the entries
+ *               of d_streams and d_in_bytes at local_pos are not read.  NULL:
+ *               all S inputs are streams, as in zccl_decompress_reduce.
+ *   accumulate: nonzero: the fold starts from the BF16 values already in
+ *               d_out, so d_out[i] = RNE_bf16(((d_out[i] + x_0[i]) + ...) +
+ *               x_{S-1}[i]); zero: as zccl_decompress_reduce.
+ * Adds, rounding, NaN rule, errors and workspace as zccl_decompress_reduce
+ * (workspace: zccl_workspace_bytes(ZCCL_OP_DECOMPRESS_REDUCE, n, S)). */
+zccl_status_t zccl_decompress_reduce_local(const void* const* d_streams, const uint64_t* d_in_bytes,
+                                           uint32_t S, const uint16_t* d_local, uint32_t local_pos,
+                                           int accumulate, uint16_t* d_out, uint64_t n, void* d_ws,
+                                           uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream);
+
 /* Diagnostic of the bounded device waits.  The kernels' only waits are on
  * barriers completed by their own TMA copies; each gives up after a limit
  * and reports ZCCL_ERR_TIMEOUT rather than hang.  This call runs that same

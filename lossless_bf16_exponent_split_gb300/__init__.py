@@ -53,6 +53,10 @@ _SIGS = {
     "zccl_decompress_reduce": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
                                 ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                 ctypes.c_void_p], ctypes.c_int),
+    "zccl_decompress_reduce_local": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p,
+                                      ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64,
+                                      ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p],
+                                     ctypes.c_int),
     "zccl_decompress_noalloc": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
                                  ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_check_bounded_wait": ([ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
@@ -139,6 +143,15 @@ def zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes, d
                            stream) -> int:
     return lib().zccl_decompress_reduce(d_streams, d_in_bytes, S, d_out, n, d_ws, ws_bytes,
                                         d_status, stream)
+
+
+def zccl_decompress_reduce_local(d_streams, d_in_bytes, S, d_local, local_pos, accumulate, d_out, n, d_ws,
+                                 ws_bytes, d_status, stream) -> int:
+    """zccl_decompress_reduce with the rank's own shard as plain BF16 at
+    local_pos (d_local may be 0 for none) and, with accumulate, the fold
+    starting from the values already in d_out."""
+    return lib().zccl_decompress_reduce_local(d_streams, d_in_bytes, S, d_local, local_pos, accumulate, d_out,
+                                              n, d_ws, ws_bytes, d_status, stream)
 
 
 def zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream) -> int:

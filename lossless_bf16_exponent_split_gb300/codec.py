@@ -12,7 +12,8 @@ import torch
 
 from . import (OP_COMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS, OP_DECOMPRESS_REDUCE, OK,
                ZcclError, check, zccl_compress, zccl_compress_batched, zccl_decompress,
-               zccl_decompress_reduce, zccl_max_compressed_bytes, zccl_workspace_bytes)
+               zccl_decompress_reduce, zccl_decompress_reduce_local, zccl_max_compressed_bytes,
+               zccl_workspace_bytes)
 
 SEGMENT_DTYPE = np.dtype([("in", "<u8"), ("n", "<u8"), ("out", "<u8"), ("cap", "<u8")])
 
@@ -119,4 +120,28 @@ class Codec:
                                      self.status.data_ptr(), _stream_handle(self.stream)),
               "zccl_decompress_reduce")
         self._keep = (ptrs, in_bytes)  # alive until the next call
+        return out
+
+    def decompress_reduce_local(self, streams, in_bytes, n: int, local: torch.Tensor | None = None,
+                                local_pos: int = 0, out: torch.Tensor | None = None, accumulate: bool = False):
+        """Like decompress_reduce, with the rank's own shard `local` (plain
+        BF16, 16-bit tensor) at position local_pos (its entry in `streams`
+        is ignored and may be None) and, with accumulate, the fold starting
+        from the values already in `out`."""
+        S = len(streams)
+        ptrs = torch.tensor([0 if st is None else st.data_ptr() for st in streams], dtype=torch.int64)
+        ptrs = ptrs.to(self.device)
+        if not torch.is_tensor(in_bytes):
+            in_bytes = torch.tensor([int(v) for v in in_bytes], dtype=torch.int64).to(self.device)
+        if out is None:
+            if accumulate:
+                raise ValueError("accumulate needs an existing out")
+            out = torch.empty(max(n, 1), dtype=torch.int16, device=self.device)[:n]
+        ws, wsb = self.workspace(zccl_workspace_bytes(OP_DECOMPRESS_REDUCE, n, S))
+        check(zccl_decompress_reduce_local(ptrs.data_ptr(), in_bytes.data_ptr(), S,
+                                           _as_u16_ptr(local) if local is not None and n else 0, local_pos,
+                                           1 if accumulate else 0, out.data_ptr() if n else 0, n, ws, wsb,
+                                           self.status.data_ptr(), _stream_handle(self.stream)),
+              "zccl_decompress_reduce_local")
+        self._keep = (ptrs, in_bytes)
         return out

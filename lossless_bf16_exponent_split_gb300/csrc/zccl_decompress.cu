@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
         const uint32_t s = r / rps, q = r % rps;
         if (tid == 0) {
             uint64_t n_esc;
-            sm.hdr_ok = stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc);
+            // (the plain BF16 position, if any, has no stream: zero counts)
+            sm.hdr_ok = s != a.skip && stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc);
         }
         __syncthreads();
         const uint32_t c0 = q * kRangeChunks;
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
         // every stream's recount must equal its header's escape count
         for (uint32_t s = tid; s < a.S; s += kThreads) {
             uint64_t n_esc = 0;
+            if (s == a.skip) continue;
             if (!stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc)) {
                 report(a.status, ZCCL_ERR_CORRUPT_STREAM);
             } else if (rps > 0) {

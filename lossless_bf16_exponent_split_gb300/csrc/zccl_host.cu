@@ -268,13 +268,18 @@ zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_o
                : ZCCL_ERR_CUDA;
 }
 
-zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
-                                     uint16_t* d_out, uint64_t n, void* d_ws, uint64_t ws_bytes,
-                                     uint32_t* d_status, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+zccl_status_t reduce_impl(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
+                          const uint16_t* d_local, uint32_t local_pos, int accumulate, uint16_t* d_out, uint64_t n,
+                          void* d_ws, uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream)
 {
     if (S == 0 || S > ZCCL_MAX_SHARDS || n >= kMaxElems || d_streams == nullptr || !aligned(d_streams, 8) ||
         d_in_bytes == nullptr || !aligned(d_in_bytes, 8) || (n > 0 && (d_out == nullptr || !aligned(d_out, 16))) ||
-        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4) ||
+        (d_local != nullptr && (local_pos >= S || !aligned(d_local, 16))))
         return ZCCL_ERR_INVALID_ARG;
     const uint64_t units = units_of(n);
     const ScanLayout l = scan_layout(units, S);
@@ -286,6 +291,7 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
     sc.streams = d_streams;
     sc.in_bytes_dev = d_in_bytes;
     sc.S = S;
+    sc.skip = d_local != nullptr ? local_pos : S;
     sc.n = n;
     sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
     sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
@@ -297,11 +303,14 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
     a.streams = d_streams;
     a.in_bytes = d_in_bytes;
     a.S = S;
+    a.local = d_local;
+    a.local_pos = d_local != nullptr ? local_pos : 0u;
+    a.accumulate = accumulate ? 1u : 0u;
     a.out = d_out;
     a.n = n;
     a.ctrl = sc.ctrl;
     a.bases = sc.bases;
-    a.local = sc.local;
+    a.local_off = sc.local;
     a.count = sc.count;
     a.status = d_status;
     const int per_sm = S <= kSmallShards ? dev->reduce_per_sm_small : dev->reduce_per_sm_large;
@@ -309,6 +318,26 @@ zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_
                          grid_for(units, per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+zccl_status_t zccl_decompress_reduce(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
+                                     uint16_t* d_out, uint64_t n, void* d_ws, uint64_t ws_bytes,
+                                     uint32_t* d_status, cudaStream_t stream)
+{
+    return reduce_impl(d_streams, d_in_bytes, S, nullptr, 0, 0, d_out, n, d_ws, ws_bytes, d_status, stream);
+}
+
+zccl_status_t zccl_decompress_reduce_local(const void* const* d_streams, const uint64_t* d_in_bytes, uint32_t S,
+                                           const uint16_t* d_local, uint32_t local_pos, int accumulate,
+                                           uint16_t* d_out, uint64_t n, void* d_ws, uint64_t ws_bytes,
+                                           uint32_t* d_status, cudaStream_t stream)
+{
+    return reduce_impl(d_streams, d_in_bytes, S, d_local, local_pos, accumulate, d_out, n, d_ws, ws_bytes,
+                       d_status, stream);
 }
 
 zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream)

@@ -34,6 +34,7 @@ struct ScanArgs {
     const uint64_t* in_bytes_dev;  // device [S], or nullptr with `in_bytes`
     uint64_t in_bytes;
     uint32_t S;
+    uint32_t skip;               // a position holding plain BF16 (no stream), or S for none
     uint64_t n;
     WsCtrl* ctrl;
     uint32_t* totals;            // [S][ranges per stream] escapes per range
@@ -58,11 +59,14 @@ struct ReduceArgs {
     const void* const* streams;  // device [S]
     const uint64_t* in_bytes;    // device [S]
     uint32_t S;
+    const uint16_t* local;       // plain BF16 input at position local_pos, or nullptr
+    uint32_t local_pos;
+    uint32_t accumulate;         // nonzero: the fold starts from the values in out
     uint16_t* out;
     uint64_t n;
     WsCtrl* ctrl;
     uint64_t* bases;             // from the scan: [S][ranges per stream] (cleared by the last CTA)
-    uint32_t* local;             // [S][units] (each cleared once read)
+    uint32_t* local_off;         // [S][units] chunk prefix within its range (each cleared once read)
     uint32_t* count;             // [S][units] (each cleared once read)
     uint32_t* status;
 };

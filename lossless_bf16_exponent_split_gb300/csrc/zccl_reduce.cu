@@ -34,9 +34,16 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kStages = 3;
 
+// One stage of the ring: a shard's block and its zero-point run, or a chunk
+// of plain BF16 (the rank's own shard, or the output being accumulated into).
+struct __align__(16) Stage {
+    uint8_t blk[kBlockBytes];
+    uint8_t zpb[kZpBufBytes];
+};
+static_assert(sizeof(Stage) >= 2 * kChunk, "a chunk of plain BF16 fits a stage");
+
 struct __align__(16) ReduceSmem {
-    uint8_t blk[kStages][kBlockBytes];
-    uint8_t zpb[kStages][kZpBufBytes];
+    Stage stage[kStages];
     uint8_t expo[kChunk];
     uint64_t bar[kStages];
     uint32_t zdelta[kStages];
@@ -63,9 +70,28 @@ __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t 
     return t;
 }
 
-// Offsets of one step's zero-point run: the range base plus the chunk's
-// prefix within its range, and its escape count (loaded one iteration ahead
-// of their use by issue_step, so thread 0 never waits on them).
+// The steps of an output chunk: (accumulating) the output's current values,
+// then the S inputs in rank order -- each a shard's compressed stream, or
+// the plain BF16 of the rank's own shard at local_pos.
+enum : uint32_t { kStepStream = 0, kStepLocal = 1, kStepOut = 2 };
+
+__device__ __forceinline__ uint32_t steps_per_chunk(const ReduceArgs& a) { return a.S + (a.accumulate ? 1u : 0u); }
+
+// Kind of step q of a chunk; *shard gets the input position of a stream step.
+__device__ __forceinline__ uint32_t step_kind(const ReduceArgs& a, uint32_t q, uint32_t* shard)
+{
+    if (a.accumulate) {
+        if (q == 0) return kStepOut;
+        --q;
+    }
+    *shard = q;
+    return (a.local != nullptr && q == a.local_pos) ? kStepLocal : kStepStream;
+}
+
+// Offsets of one stream step's zero-point run: the range base plus the
+// chunk's prefix within its range, and its escape count (loaded one
+// iteration ahead of their use by issue_step, so thread 0 never waits on
+// them).
 struct StepOffsets {
     uint64_t base;
     uint32_t local, count;
@@ -74,27 +100,37 @@ struct StepOffsets {
 __device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t j, uint32_t total)
 {
     StepOffsets o{0, 0, 0};
-    const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
-    if (c >= total) return o;
-    const uint32_t s = j % a.S;
+    const uint32_t Q = steps_per_chunk(a);
+    const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
+    uint32_t s = 0;
+    if (c >= total || step_kind(a, j % Q, &s) != kStepStream) return o;
     const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
     const uint64_t idx = (uint64_t)s * total + c;
     o.base = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks);
-    o.local = __ldcg(a.local + idx);
+    o.local = __ldcg(a.local_off + idx);
     o.count = __ldcg(a.count + idx);
     return o;
 }
 
-// Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / S) * gridDim.x,
-// shard j % S) into stage j % kStages.
+// Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / Q) * gridDim.x,
+// step j % Q) into stage j % kStages.
 __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t j,
                                            uint32_t total, const StepOffsets& off)
 {
-    const uint32_t c = blockIdx.x + (j / a.S) * gridDim.x;
+    const uint32_t Q = steps_per_chunk(a);
+    const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
     if (c >= total) return;
-    const uint32_t s = j % a.S;
+    uint32_t s = 0;
+    const uint32_t kind = step_kind(a, j % Q, &s);
     const int st = j % kStages;
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
+    if (kind != kStepStream) {  // plain BF16: whole 16-byte pieces by bulk copy, the rest by plain loads
+        const uint16_t* src = (kind == kStepLocal ? a.local : a.out) + (uint64_t)c * kChunk;
+        const uint32_t bytes = (valid * 2) & ~15u;
+        mbar_arrive_expect_tx(&sm.bar[st], bytes);
+        if (bytes) bulk_g2s(sm.stage[st].blk, src, bytes, &sm.bar[st]);
+        return;
+    }
     const uint32_t bytes = slots_of(valid) * 11 / 8;
     const uint64_t o0 = off.base + off.local;
     const uint64_t o1 = o0 + off.count;
@@ -113,17 +149,18 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
     sm.zdelta[st] = delta;
     sm.zcount[st] = cnt;
     mbar_arrive_expect_tx(&sm.bar[st], bytes + zbytes);
-    bulk_g2s(sm.blk[st], t.base[s] + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[st]);
-    if (zbytes) bulk_g2s(sm.zpb[st], t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
+    bulk_g2s(sm.stage[st].blk, t.base[s] + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[st]);
+    if (zbytes) bulk_g2s(sm.stage[st].zpb, t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
 }
 
-// All threads of the CTA: the CTA's chunks (static stride), each over the S
-// shards in order.  The fp32 sums are kept as pairs and added with the
+// All threads of the CTA: the CTA's chunks (static stride), each over its
+// steps in order.  The fp32 sums are kept as pairs and added with the
 // two-lane add (each lane rounds to nearest even exactly as a scalar add).
 __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t total = (uint32_t)units_of(a.n);
+    const uint32_t Q = steps_per_chunk(a);
     StepOffsets ahead{0, 0, 0};  // thread 0: offsets of the next step to queue
     if (tid == 0) {
         for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total, load_offsets(a, j, total));
@@ -134,7 +171,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
 #pragma unroll
     for (int q = 0; q < 16; ++q) acc[q] = make_float2(0.0f, 0.0f);
 
-    uint32_t j = 0, s = 0, c = blockIdx.x;  // step, its shard and its chunk
+    uint32_t j = 0, q = 0, c = blockIdx.x;  // step, its place in the chunk's steps, its chunk
     for (;; ++j) {
         if (c >= total) break;
         const int st = j % kStages;
@@ -142,60 +179,73 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             issue_step(a, sm, t, j + kStages - 1, total, ahead);
             ahead = load_offsets(a, j + kStages, total);
         }
+        uint32_t s = 0;
+        const uint32_t kind = step_kind(a, q, &s);
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
         if (!mbar_wait(&sm.bar[st], (j / kStages) & 1)) atomicExch(&sm.abort, 1u);
+        uint8_t* blk = sm.stage[st].blk;
+        if (kind != kStepStream) {  // plain BF16: the last < 8 values by plain loads
+            const uint32_t done = valid & ~7u;
+            if (tid < (int)(valid - done)) {
+                const uint16_t* src = kind == kStepLocal ? a.local : a.out;
+                reinterpret_cast<uint16_t*>(blk)[done + tid] = src[first + done + tid];
+            }
+        }
         __syncthreads();
         if (sm.abort) {
             if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
             break;
         }
-        const uint8_t* blk = sm.blk[st];
-        uint32_t esc = 0;
-        if (tid < (int)(L / 32)) {
-            const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-            const uint32_t w0 = 32u * tid;
-            const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
-                                   : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-            esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
-        }
-        uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
-        if (agg == sm.zcount[st]) {
-            const uint8_t* src = sm.zpb[st] + sm.zdelta[st] + excl;
-            uint32_t m = esc, jj = 0;
-            while (m) {
-                const uint32_t b = __ffs(m) - 1;
-                m &= m - 1;
-                sm.expo[32u * tid + b] = src[jj++];
+        if (kind == kStepStream) {
+            uint32_t esc = 0;
+            if (tid < (int)(L / 32)) {
+                const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+                const uint32_t w0 = 32u * tid;
+                const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
+                                       : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+                esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
             }
-        } else if (tid == 0) {
-            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            uint32_t agg;
+            const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
+            if (agg == sm.zcount[st]) {
+                const uint8_t* src = sm.stage[st].zpb + sm.zdelta[st] + excl;
+                uint32_t m = esc, jj = 0;
+                while (m) {
+                    const uint32_t b = __ffs(m) - 1;
+                    m &= m - 1;
+                    sm.expo[32u * tid + b] = src[jj++];
+                }
+            } else if (tid == 0) {
+                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+            }
+            __syncthreads();
         }
-        __syncthreads();
         const uint32_t lut_lo = t.lut[2 * s], lut_hi = t.lut[2 * s + 1];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
             if (e0 < L) {
-                const uint4 o = decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
-                                        blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
-                                        *reinterpret_cast<const uint2*>(sm.expo + e0));
+                const uint4 o = kind == kStepStream
+                                    ? decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
+                                              blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo,
+                                              lut_hi, *reinterpret_cast<const uint2*>(sm.expo + e0))
+                                    : *reinterpret_cast<const uint4*>(blk + 2 * e0);
                 const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 f = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
-                    acc[4 * i + q] = s == 0 ? f : __fadd2_rn(acc[4 * i + q], f);
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+                    acc[4 * i + k] = q == 0 ? f : __fadd2_rn(acc[4 * i + k], f);
                 }
             }
         }
-        if (s + 1 == a.S) {
+        if (q + 1 == Q) {
             // the chunk's offset words have had their one reader (loaded
             // steps ago): clear them
-            for (uint32_t q = tid; q < a.S; q += kThreads) {
-                a.local[(uint64_t)q * total + c] = 0;
-                a.count[(uint64_t)q * total + c] = 0;
+            for (uint32_t r = tid; r < a.S; r += kThreads) {
+                a.local_off[(uint64_t)r * total + c] = 0;
+                a.count[(uint64_t)r * total + c] = 0;
             }
             uint16_t* dst = a.out + first;
 #pragma unroll
@@ -215,15 +265,15 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             }
         }
         __syncthreads();
-        if (++s == a.S) {  // next step: the next shard, or the next chunk's first
-            s = 0;
+        if (++q == Q) {  // the next chunk's first step
+            q = 0;
             c += gridDim.x;
         }
     }
     // steps still in flight after an early stop: wait for them (bounded)
     if (tid == 0 && sm.abort) {
         for (uint32_t jj = j + 1; jj < j + kStages; ++jj) {
-            if (blockIdx.x + (jj / a.S) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
+            if (blockIdx.x + (jj / Q) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
         }
     }
 }
@@ -240,6 +290,12 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
     // stops this kernel from reading out of bounds)
     bool ok = true;
     for (uint32_t s = tid; s < a.S; s += kThreads) {
+        if (a.local != nullptr && s == a.local_pos) {  // the plain BF16 input: no stream
+            t.base[s] = nullptr;
+            t.n_esc[s] = 0;
+            t.lut[2 * s] = t.lut[2 * s + 1] = 0;
+            continue;
+        }
         const uint8_t* base = reinterpret_cast<const uint8_t*>(a.streams[s]);
         const uint64_t in_bytes = a.in_bytes[s];
         bool good = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
@@ -268,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
     } else {  // a bad header: nothing to decode, but leave the scratch clear
         for (uint32_t c = blockIdx.x; c < total; c += gridDim.x)
             for (uint32_t s = tid; s < a.S; s += kThreads) {
-                a.local[(uint64_t)s * total + c] = 0;
+                a.local_off[(uint64_t)s * total + c] = 0;
                 a.count[(uint64_t)s * total + c] = 0;
             }
     }

@@ -134,4 +134,7 @@ CONFIGS = {
                     desc="16384 tokens x top-8 of 64 experts (Zipf 1.2), hidden 2048, N(0,1)"),
     "rs_local": dict(S=8, n=16_777_216, sigma=1e-3,
                      desc="8 shards x 16,777,216 BF16 N(0, 1e-3^2)"),
+    # the same shards as one rank (position 3) sees them: its own shard stays uncompressed
+    "rs_local_own": dict(S=8, n=16_777_216, sigma=1e-3, local_pos=3,
+                         desc="8 shards x 16,777,216 BF16 N(0, 1e-3^2); shard 3 is the rank's own, plain BF16"),
 }

@@ -85,6 +85,11 @@ def test_argument_errors_need_no_gpu(z):
     assert z.zccl_compress(**dict(ok, ws_bytes=64)) == z.BUFFER_TOO_SMALL
     assert z.zccl_decompress(A, 64, A, 4096, A, 1 << 16, 0, None) == z.INVALID_ARG  # in_bytes too small
     assert z.zccl_decompress_reduce(A, A, 0, A, 100, A, 1 << 16, 0, None) == z.INVALID_ARG
+    wsr = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, 100, 4)
+    assert z.zccl_decompress_reduce_local(A, A, 4, A, 4, 0, A, 100, A, wsr, 0, None) == z.INVALID_ARG  # local_pos >= S
+    assert z.zccl_decompress_reduce_local(A, A, 4, A + 8, 1, 0, A, 100, A, wsr, 0, None) == z.INVALID_ARG  # unaligned
+    assert z.zccl_decompress_reduce_local(A, A, 0, A, 0, 1, A, 100, A, wsr, 0, None) == z.INVALID_ARG  # S == 0
+    assert z.zccl_decompress_reduce_local(A, A, 4, A, 1, 1, A, 100, A, 64, 0, None) == z.BUFFER_TOO_SMALL
     assert z.zccl_compress_batched(A, 0, 100, lut, A, A, 1 << 16, 0, None) == z.INVALID_ARG
     assert z.zccl_status_string(0) == "ok"
     assert z.status_string(z.CORRUPT_STREAM) == "corrupt stream"

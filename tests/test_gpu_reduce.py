@@ -74,3 +74,59 @@ def test_rs_local_full(codec):
     st, got = gpu_reduce(codec, streams, cfg["n"])
     assert st == 0
     assert np.array_equal(got, want)
+
+
+def gpu_reduce_local(codec, streams, n, local, local_pos, initial=None):
+    devs = [None if s is None else dev_bytes(s) for s in streams]
+    sizes = [0 if s is None else len(s) for s in streams]
+    dlocal = None if local is None else torch.from_numpy(np.ascontiguousarray(local, np.uint16).view(np.int16)).cuda()
+    out = None
+    if initial is not None:
+        out = torch.from_numpy(np.ascontiguousarray(initial, np.uint16).view(np.int16)).cuda()
+    codec.reset_status()
+    out = codec.decompress_reduce_local(devs, sizes, n, local=dlocal, local_pos=local_pos, out=out,
+                                        accumulate=initial is not None)
+    torch.cuda.synchronize()
+    return codec.read_status(), host_u16(out)
+
+
+@pytest.mark.parametrize("S,n,local_pos,acc", [(1, 5000, 0, False), (1, 4099, 0, True), (2, 4096, 1, False),
+                                               (3, 3 * 4096 + 77, 0, True), (5, 100_003, 2, False),
+                                               (8, 65_541, 7, True), (4, 7, 3, True), (6, 20_000, 5, False)])
+def test_reduce_local_shard_matches_oracle(codec, S, n, local_pos, acc):
+    """ZipCCL 2.D as one rank runs it: the rank's own shard enters the fold
+    uncompressed at its rank position; optionally the fold starts from the
+    output's current values.  Ragged n exercises the plain-BF16 tail."""
+    shards = [workloads.special_values(n, seed=100 * S + s, frac=0.05) for s in range(S)]
+    lut = oracle.lut_from_sigma(1.0)
+    streams = [None if s == local_pos else oracle.compress(x, lut) for s, x in enumerate(shards)]
+    initial = workloads.special_values(n, seed=7 + S, frac=0.05) if acc else None
+    want = oracle.decompress_reduce_local(streams, n, local=shards[local_pos], local_pos=local_pos, initial=initial)
+    st, got = gpu_reduce_local(codec, streams, n, shards[local_pos], local_pos, initial)
+    assert st == 0
+    assert np.array_equal(got, want)
+
+
+def test_reduce_accumulate_without_local(codec):
+    n, S = 2 * 4096 + 5, 3
+    shards = [workloads.gaussian(n, 1e-3, seed=40 + s) for s in range(S)]
+    lut = oracle.lut_from_sigma(1e-3)
+    streams = [oracle.compress(x, lut) for x in shards]
+    initial = workloads.gaussian(n, 1e-3, seed=99)
+    want = oracle.decompress_reduce_local(streams, n, initial=initial)
+    st, got = gpu_reduce_local(codec, streams, n, None, 0, initial)
+    assert st == 0
+    assert np.array_equal(got, want)
+
+
+def test_reduce_local_equals_all_compressed(codec):
+    """Holding one's own shard uncompressed gives the same bits as receiving
+    it compressed (the codec is lossless)."""
+    n, S = 50_000, 4
+    shards = [workloads.gaussian(n, 1e-3, seed=60 + s) for s in range(S)]
+    lut = oracle.lut_from_sigma(1e-3)
+    streams = [oracle.compress(x, lut) for x in shards]
+    st0, all_c = gpu_reduce(codec, streams, n)
+    st1, with_local = gpu_reduce_local(codec, [streams[0], None, streams[2], streams[3]], n, shards[1], 1)
+    assert st0 == 0 and st1 == 0
+    assert np.array_equal(all_c, with_local)
