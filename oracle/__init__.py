@@ -69,6 +69,8 @@ def _load():
                                       ctypes.c_uint64], ctypes.c_int),
             "zo_decompress_reduce_local": ([ctypes.POINTER(u8p), u64p, ctypes.c_uint32, u16p, ctypes.c_uint32,
                                             ctypes.c_int, u16p, ctypes.c_uint64], ctypes.c_int),
+            "zo_exponent_histogram": ([u16p, ctypes.c_uint64, u64p], None),
+            "zo_lut_from_histogram": ([u64p, u8p], ctypes.c_int),
             "zo_round_bf16": ([ctypes.c_float], ctypes.c_uint16),
             "zo_round_bf16_n": ([ctypes.POINTER(ctypes.c_float), u16p, ctypes.c_uint64], None),
         }
@@ -206,3 +208,22 @@ def round_bf16_array(f: np.ndarray) -> np.ndarray:
     out = np.zeros(max(f.size, 1), np.uint16)
     _load().zo_round_bf16_n(_ptr(f, ctypes.c_float), _ptr(out, ctypes.c_uint16), f.size)
     return out[: f.size]
+
+
+def exponent_histogram(x) -> np.ndarray:
+    """hist[e] = number of BF16 values with biased exponent e (0..255)."""
+    x = np.ascontiguousarray(np.asarray(x, np.uint16))
+    hist = np.zeros(256, np.uint64)
+    buf = x if x.size else np.zeros(1, np.uint16)
+    _load().zo_exponent_histogram(_ptr(buf, ctypes.c_uint16), x.size, _ptr(hist, ctypes.c_uint64))
+    return hist
+
+
+def lut_from_histogram(hist) -> bytes:
+    """The 7 most frequent exponents, rank order, ties to the smaller one."""
+    h = np.ascontiguousarray(np.asarray(hist, np.uint64))
+    lut = np.zeros(7, np.uint8)
+    st = _load().zo_lut_from_histogram(_ptr(h, ctypes.c_uint64), _ptr(lut, ctypes.c_uint8))
+    if st != OK:
+        raise OracleError(st, "lut_from_histogram")
+    return lut.tobytes()

@@ -399,3 +399,32 @@ int zo_decompress_reduce_local(const uint8_t* const* in, const uint64_t* in_byte
     free(dec);
     return st;
 }
+
+/* Exponent histogram of n BF16 values: hist[e] = how many have biased
+ * exponent e (bits 7..14), for e = 0..255.  hist is overwritten. */
+void zo_exponent_histogram(const uint16_t* x, uint64_t n, uint64_t hist[256])
+{
+    for (int e = 0; e < 256; e++) hist[e] = 0;
+    for (uint64_t i = 0; i < n; i++) hist[(x[i] >> 7) & 0xFF]++;
+}
+
+/* A LUT measured from data, the alternative to the sigma rule that the page
+ * sets aside for cost (ZipCCL 2.A: no online statistics pass) [R15]: the 7
+ * exponents with the largest counts, in rank order (code 1 = most frequent),
+ * ties to the smaller exponent; every exponent 0..255 is a candidate (a
+ * data LUT may hold the zero/subnormal binade, unlike the sigma rule). */
+int zo_lut_from_histogram(const uint64_t hist[256], uint8_t lut[7])
+{
+    if (hist == NULL || lut == NULL) return ZO_INVALID_ARG;
+    int taken[256] = {0};
+    for (int r = 0; r < 7; r++) {
+        int best = -1;
+        for (int e = 0; e < 256; e++) {
+            if (taken[e]) continue;
+            if (best < 0 || hist[e] > hist[best]) best = e;  /* strict: the smaller e wins ties */
+        }
+        taken[best] = 1;
+        lut[r] = (uint8_t)best;
+    }
+    return ZO_OK;
+}
