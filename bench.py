@@ -10,10 +10,12 @@ buffer sets, 316 MB touched per step (> 129 MB L2), keep every step's inputs
 out of L2.  Other workloads (--workload): activation_mix (compress +
 decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
 rs_local (decompress-reduce of 8 shards), rs_local_own (the same with the rank's own shard
-uncompressed), gauss1m.
+uncompressed), activation_mix_lut (the exponent histogram pass that measures
+a LUT from the data), gauss1m.
 
 Prints ONE JSON line (rank 0).  `value` = GB/s of BF16 input through the step
-(2n bytes per compress and per decompress; reduce: 2 S n), whole job.
+(2n bytes per compress and per decompress; reduce: 2 S n; histogram: 2n),
+whole job.
 `--impl reference` times the CPU oracle (plain C, single thread) instead.
 """
 from __future__ import annotations
@@ -44,7 +46,7 @@ def parse_args():
     p.add_argument("--impl", default="zccl", choices=["zccl", "reference"])
     p.add_argument("--workload", default="llama3_8b_allgather",
                    choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "rs_local_own",
-                            "gauss1m"])
+                            "activation_mix_lut", "gauss1m"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -73,15 +75,17 @@ def source_sha(names):
 
 # the kernels of each op live in these sources (plus zccl_common.cuh)
 KERNEL_SOURCES = {"compress": ["zccl_compress.cu"], "decompress": ["zccl_decompress.cu", "zccl_decode.cuh"],
-                  "decompress_reduce": ["zccl_reduce.cu", "zccl_decompress.cu", "zccl_decode.cuh"]}
+                  "decompress_reduce": ["zccl_reduce.cu", "zccl_decompress.cu", "zccl_decode.cuh"],
+                  "histogram": ["zccl_hist.cu"]}
 OP_KERNELS = {"compress": "compress_kernel (one cooperative launch)",
               "decompress": "decompress_kernel (one cooperative launch)",
-              "decompress_reduce": "escape_scan_kernel + reduce_kernel (PDL pair)"}
-OP_LAUNCHES = {"compress": 1, "decompress": 1, "decompress_reduce": 2}
+              "decompress_reduce": "escape_scan_kernel + reduce_kernel (PDL pair)",
+              "histogram": "hist_zero_kernel + hist_kernel (PDL pair)"}
+OP_LAUNCHES = {"compress": 1, "decompress": 1, "decompress_reduce": 2, "histogram": 2}
 # the committed ncu summary of each op's dominant kernel is
 # profiles/<PROFILE_KERNEL[op]>_<workload>.md
 PROFILE_KERNEL = {"compress": "compress_kernel", "decompress": "decompress_kernel",
-                  "decompress_reduce": "reduce_kernel"}
+                  "decompress_reduce": "reduce_kernel", "histogram": "hist_kernel"}
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -206,6 +210,8 @@ def make_inputs(name, seed):
         return "roundtrip", w.gaussian(cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"], None
     if name == "activation_mix":
         return "roundtrip", w.activation_mix(seed=seed), cfg["sigma"], None
+    if name == "activation_mix_lut":
+        return "histogram", w.activation_mix(seed=seed), cfg["sigma"], None
     if name == "moe_a2a":
         m = w.moe_payload(tokens=cfg["tokens"], top_k=cfg["top_k"], experts=cfg["experts"],
                           hidden=cfg["hidden"], seed=seed)
@@ -241,8 +247,20 @@ def cpu_baseline(name, budget_s=12.0):
         dt = (time.perf_counter() - t0) / reps
         return {"value": round(2 * cfg["S"] * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": f"decompress_reduce of {cfg['S']} shards x {n} elements, {reps} reps"}
+    if name == "activation_mix_lut":
+        x = w.activation_mix(2048, 4096)
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.lut_from_histogram(oracle.exponent_histogram(x))
+            reps += 1
+            if time.perf_counter() - t0 > budget_s / 2:
+                break
+        dt = (time.perf_counter() - t0) / reps
+        return {"value": round(2 * x.size / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"exponent histogram + LUT of the first {x.size} elements of the workload, {reps} reps"}
     n = 1 << 23
-    x = w.gaussian(n, sigma, seed=0) if name != "activation_mix" else w.activation_mix(2048, 4096)
+    x = w.gaussian(n, sigma, seed=0) if not name.startswith("activation_mix") else w.activation_mix(2048, 4096)
     n = x.size
     t0 = time.perf_counter()
     reps = 0
@@ -281,6 +299,11 @@ def run_reference(args):
             step = lambda: oracle.decompress_reduce_local(streams, n, local=shards[lp], local_pos=lp)
         unit_bytes = 2 * cfg["S"] * n
         sample = f"decompress_reduce of {cfg['S']} shards x {n} elements per step"
+    elif cfg_name == "activation_mix_lut":
+        x = w.activation_mix(1024, 4096)
+        step = lambda: oracle.lut_from_histogram(oracle.exponent_histogram(x))
+        unit_bytes = 2 * x.size
+        sample = f"exponent histogram + LUT of {x.size} elements of the workload per step"
     else:
         n = 1 << 21
         x = w.gaussian(n, cfg["sigma"], seed=0)
@@ -413,6 +436,34 @@ def main():
         cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
                      "step": "one batched compress of all static+dynamic segments",
                      "l2": "input 537 MB > 129 MB L2"}
+    elif kind == "histogram":
+        n = host.size
+        R = 5
+        xs = [tdev(host) for _ in range(R)]
+        hist = torch.empty(256, dtype=torch.int64, device=dev)
+
+        def hist_call(r):
+            z.check(z.zccl_exponent_histogram(xs[r].data_ptr(), n, hist.data_ptr(), 0, h), "exponent_histogram")
+        names = ["histogram"]
+        alg = {"histogram": 2 * n + 256 * 8}
+        step_input_bytes = 2 * n
+
+        def step(k, ev=None):
+            if ev:
+                ev[0].record(stream)
+            hist_call(k % R)
+            if ev:
+                ev[1].record(stream)
+                ev[2].record(stream)
+        hist_call(0)
+        hh0 = hist.cpu().numpy().view(np.uint64).astype(np.float64)
+        lut_data = z.zccl_lut_from_histogram(hist.cpu().numpy().view(np.uint64))
+        coverage = {"sigma_lut": round(float(hh0[list(lut)].sum() / n), 6),
+                    "data_lut": round(float(hh0[list(lut_data)].sum() / n), 6),
+                    "sigma": sigma, "data_lut_exponents": list(lut_data)}
+        cfg_extra = {"n": n, "step": "one exponent histogram pass (zeroing + counting kernel, PDL pair)",
+                     "top7_coverage": coverage,
+                     "l2": f"5 rotating inputs; {4 * 2 * n >> 20} MiB read between two reads of one (> 129 MB L2)"}
     else:  # reduce (with the rank's own shard uncompressed at local_pos, if given)
         shards = host
         local_pos = extra
@@ -523,6 +574,32 @@ def main():
         e2e = {"value": round(world * 2 * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 8,
                "path": "pinned host -> H2D -> zccl_compress -> zccl_decompress -> D2H"}
+
+    if kind == "histogram" and not args.no_e2e:
+        hx = torch.from_numpy(host.view(np.int16)).pin_memory()
+        hh = torch.empty(256, dtype=torch.int64).pin_memory()
+        luts = []
+
+        def e2e_step():
+            xs[0].copy_(hx, non_blocking=True)
+            hist_call(0)
+            hh.copy_(hist, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            luts.append(z.zccl_lut_from_histogram(hh.numpy().view(np.uint64)))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(pg, dev)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+        e2e_ms = max_over_ranks(pg, e2e_ms, dev)
+        assert len(set(luts)) == 1
+        e2e = {"value": round(world * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 256 * 8,
+               "path": "pinned host -> H2D -> zccl_exponent_histogram -> D2H -> zccl_lut_from_histogram",
+               "lut": list(luts[0])}
 
     if rank != 0:
         return

@@ -187,6 +187,31 @@ zccl_status_t zccl_decompress_reduce_local(const void* const* d_streams, const u
                                            int accumulate, uint16_t* d_out, uint64_t n, void* d_ws,
                                            uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream);
 
+/* Exponent histogram of n BF16 values: d_hist[e] (device, 256 uint64_t,
+ * 8-byte aligned) = how many of them have biased exponent e.  accumulate = 0
+ * overwrites d_hist; accumulate != 0 adds the counts to those already there
+ * (one histogram over several tensors, e.g. a bucket sharing one LUT).  For a
+ * LUT measured from the data rather than derived from sigma (ZipCCL 2.A
+ * derives it from sigma precisely to avoid this statistics pass; the measured
+ * LUT covers at least as many values on any payload).  d_in 16-byte aligned
+ * unless n == 0; n < 2^40.  Asynchronous on `stream`; no workspace. */
+zccl_status_t zccl_exponent_histogram(const uint16_t* d_in, uint64_t n, uint64_t* d_hist, int accumulate,
+                                      cudaStream_t stream);
+
+/* Host: the LUT of the 7 most frequent exponents of a histogram (256 host
+ * uint64_t, e.g. copied back from zccl_exponent_histogram), in rank order
+ * (code 1 = most frequent), ties to the smaller exponent.  Any exponent may
+ * enter, including 0 (zeros and subnormals) and 255. */
+zccl_status_t zccl_lut_from_histogram(const uint64_t* hist, zccl_lut_t* lut);
+
+/* The measured LUT of n BF16 values in one call: zccl_exponent_histogram into
+ * d_hist (device scratch, 256 uint64_t, 8-byte aligned; holds the histogram
+ * on return), a copy back and zccl_lut_from_histogram.  Synchronises
+ * `stream`; *lut (host) is written on ZCCL_OK only.  Same argument rules as
+ * zccl_exponent_histogram. */
+zccl_status_t zccl_lut_from_data(const uint16_t* d_in, uint64_t n, uint64_t* d_hist, zccl_lut_t* lut,
+                                 cudaStream_t stream);
+
 /* Diagnostic of the bounded device waits.  The kernels' only waits are on
  * barriers completed by their own TMA copies; each gives up after a limit
  * and reports ZCCL_ERR_TIMEOUT rather than hang.  This call runs that same

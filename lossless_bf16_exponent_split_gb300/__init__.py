@@ -60,6 +60,11 @@ _SIGS = {
     "zccl_decompress_noalloc": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
                                  ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_check_bounded_wait": ([ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "zccl_exponent_histogram": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int,
+                                 ctypes.c_void_p], ctypes.c_int),
+    "zccl_lut_from_histogram": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "zccl_lut_from_data": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                           ctypes.c_int),
     "zccl_status_string": ([ctypes.c_int], ctypes.c_char_p),
 }
 
@@ -152,6 +157,31 @@ def zccl_decompress_reduce_local(d_streams, d_in_bytes, S, d_local, local_pos, a
     starting from the values already in d_out."""
     return lib().zccl_decompress_reduce_local(d_streams, d_in_bytes, S, d_local, local_pos, accumulate, d_out,
                                               n, d_ws, ws_bytes, d_status, stream)
+
+
+def zccl_exponent_histogram(d_in, n, d_hist, accumulate, stream) -> int:
+    """256 uint64 exponent counts of n BF16 values into device d_hist
+    (added to the counts there when accumulate is true)."""
+    return lib().zccl_exponent_histogram(d_in, n, d_hist, 1 if accumulate else 0, stream)
+
+
+def zccl_lut_from_histogram(hist) -> bytes:
+    """The 7 most frequent exponents of a host histogram (256 counts)."""
+    import numpy as _np
+    h = _np.ascontiguousarray(_np.asarray(hist, _np.uint64))
+    if h.size != 256:
+        raise ValueError("a histogram has 256 counts")
+    lut = (ctypes.c_uint8 * 7)()
+    check(lib().zccl_lut_from_histogram(h.ctypes.data, ctypes.addressof(lut)), "zccl_lut_from_histogram")
+    return bytes(lut)
+
+
+def zccl_lut_from_data(d_in, n, d_hist, stream) -> bytes:
+    """The measured LUT of n BF16 values (d_hist: 2 KB device scratch);
+    synchronises the stream."""
+    lut = (ctypes.c_uint8 * 7)()
+    check(lib().zccl_lut_from_data(d_in, n, d_hist, ctypes.addressof(lut), stream), "zccl_lut_from_data")
+    return bytes(lut)
 
 
 def zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream) -> int:

@@ -12,8 +12,8 @@ import torch
 
 from . import (OP_COMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS, OP_DECOMPRESS_REDUCE, OK,
                ZcclError, check, zccl_compress, zccl_compress_batched, zccl_decompress,
-               zccl_decompress_reduce, zccl_decompress_reduce_local, zccl_max_compressed_bytes,
-               zccl_workspace_bytes)
+               zccl_decompress_reduce, zccl_decompress_reduce_local, zccl_exponent_histogram,
+               zccl_lut_from_histogram, zccl_max_compressed_bytes, zccl_workspace_bytes)
 
 SEGMENT_DTYPE = np.dtype([("in", "<u8"), ("n", "<u8"), ("out", "<u8"), ("cap", "<u8")])
 
@@ -145,3 +145,22 @@ class Codec:
               "zccl_decompress_reduce_local")
         self._keep = (ptrs, in_bytes)
         return out
+
+    def exponent_histogram(self, x: torch.Tensor, hist: torch.Tensor | None = None,
+                           accumulate: bool = False) -> torch.Tensor:
+        """256 exponent counts of the BF16 tensor x, as an int64 device tensor
+        (the library writes unsigned 64-bit counts); with accumulate, added
+        to the counts already in `hist`."""
+        if hist is None:
+            if accumulate:
+                raise ValueError("accumulate needs an existing hist")
+            hist = torch.empty(256, dtype=torch.int64, device=self.device)
+        n = x.numel()
+        check(zccl_exponent_histogram(_as_u16_ptr(x) if n else 0, n, hist.data_ptr(), accumulate,
+                                      _stream_handle(self.stream)), "zccl_exponent_histogram")
+        return hist
+
+    def lut_from_data(self, x: torch.Tensor) -> bytes:
+        """The LUT of x's 7 most frequent exponents (one histogram pass on the
+        device, the selection on the host)."""
+        return zccl_lut_from_histogram(self.exponent_histogram(x).cpu().numpy().view(np.uint64))

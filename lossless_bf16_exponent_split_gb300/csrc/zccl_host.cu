@@ -340,6 +340,45 @@ zccl_status_t zccl_decompress_reduce_local(const void* const* d_streams, const u
                        d_status, stream);
 }
 
+zccl_status_t zccl_exponent_histogram(const uint16_t* d_in, uint64_t n, uint64_t* d_hist, int accumulate,
+                                      cudaStream_t stream)
+{
+    if (n >= kMaxElems || (n > 0 && (d_in == nullptr || !aligned(d_in, 16))) || d_hist == nullptr ||
+        !aligned(d_hist, 8))
+        return ZCCL_ERR_INVALID_ARG;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+    return launch_histogram(d_in, n, d_hist, accumulate != 0, dev->sms, stream) == cudaSuccess ? ZCCL_OK
+                                                                                           : ZCCL_ERR_CUDA;
+}
+
+zccl_status_t zccl_lut_from_histogram(const uint64_t* hist, zccl_lut_t* lut)
+{
+    if (hist == nullptr || lut == nullptr) return ZCCL_ERR_INVALID_ARG;
+    bool used[256] = {};
+    for (int r = 0; r < 7; ++r) {  // rank r: the largest count not yet taken, the smaller exponent on ties
+        int pick = -1;
+        for (int e = 0; e < 256; ++e)
+            if (!used[e] && (pick < 0 || hist[e] > hist[pick])) pick = e;
+        used[pick] = true;
+        lut->exp[r] = (uint8_t)pick;
+    }
+    return ZCCL_OK;
+}
+
+zccl_status_t zccl_lut_from_data(const uint16_t* d_in, uint64_t n, uint64_t* d_hist, zccl_lut_t* lut,
+                                 cudaStream_t stream)
+{
+    if (lut == nullptr) return ZCCL_ERR_INVALID_ARG;
+    const zccl_status_t st = zccl_exponent_histogram(d_in, n, d_hist, 0, stream);
+    if (st != ZCCL_OK) return st;
+    uint64_t hist[256];
+    if (cudaMemcpyAsync(hist, d_hist, sizeof(hist), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return ZCCL_ERR_CUDA;
+    return zccl_lut_from_histogram(hist, lut);
+}
+
 zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream)
 {
     if (d_status == nullptr || !aligned(d_status, 4) || limit_us == 0 || limit_us > 1000000)

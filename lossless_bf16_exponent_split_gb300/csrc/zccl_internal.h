@@ -128,6 +128,9 @@ cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_
                           cudaStream_t stream);
 int reduce_ctas_per_sm(uint32_t S);
 
+cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint64_t* hist, bool accumulate, int sms,
+                             cudaStream_t stream);
+
 cudaError_t launch_wait_check(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
 
 }  // namespace zccl

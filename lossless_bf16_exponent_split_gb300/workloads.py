@@ -137,4 +137,8 @@ CONFIGS = {
     # the same shards as one rank (position 3) sees them: its own shard stays uncompressed
     "rs_local_own": dict(S=8, n=16_777_216, sigma=1e-3, local_pos=3,
                          desc="8 shards x 16,777,216 BF16 N(0, 1e-3^2); shard 3 is the rank's own, plain BF16"),
+    # the activation payload again, for the measured-LUT statistics pass
+    "activation_mix_lut": dict(n=8192 * 4096, sigma=1.0,
+                               desc="exponent histogram + LUT of 8192x4096 BF16: 97.9% N(0,1), "
+                                    "0.1% N(0,50^2), 2% +0"),
 }

@@ -91,5 +91,29 @@ def test_argument_errors_need_no_gpu(z):
     assert z.zccl_decompress_reduce_local(A, A, 0, A, 0, 1, A, 100, A, wsr, 0, None) == z.INVALID_ARG  # S == 0
     assert z.zccl_decompress_reduce_local(A, A, 4, A, 1, 1, A, 100, A, 64, 0, None) == z.BUFFER_TOO_SMALL
     assert z.zccl_compress_batched(A, 0, 100, lut, A, A, 1 << 16, 0, None) == z.INVALID_ARG
+    assert z.zccl_exponent_histogram(A + 2, 100, A, 0, None) == z.INVALID_ARG  # unaligned input
+    assert z.zccl_exponent_histogram(A, 100, A + 4, 0, None) == z.INVALID_ARG  # unaligned histogram
+    assert z.zccl_exponent_histogram(A, 100, 0, 1, None) == z.INVALID_ARG
+    assert z.zccl_exponent_histogram(A, 1 << 40, A, 0, None) == z.INVALID_ARG
+    assert z.lib().zccl_lut_from_data(A, 100, A, 0, None) == z.INVALID_ARG  # no LUT out
+    with pytest.raises(z.ZcclError):
+        z.zccl_lut_from_data(A + 2, 100, A, None)
     assert z.zccl_status_string(0) == "ok"
     assert z.status_string(z.CORRUPT_STREAM) == "corrupt stream"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_library_lut_from_histogram_matches_oracle(z, seed):
+    """The host selection in the library against the oracle's, on histograms
+    with many ties (small counts) and with empty bins among the top 7."""
+    rng = np.random.default_rng(seed)
+    hist = rng.integers(0, 4 if seed % 2 else 1 << 40, 256, dtype=np.uint64)
+    if seed >= 4:
+        hist[:] = 0
+        hist[rng.choice(256, 3, replace=False)] = rng.integers(1, 5, 3, dtype=np.uint64)
+    assert z.zccl_lut_from_histogram(hist) == oracle.lut_from_histogram(hist)
+
+
+def test_library_lut_from_histogram_rejects_bad_size(z):
+    with pytest.raises(ValueError):
+        z.zccl_lut_from_histogram(np.zeros(255, np.uint64))

@@ -48,3 +48,21 @@ def test_data_lut_covers_at_least_the_sigma_lut(make, sigma):
     assert data_cov >= sigma_cov
     # and the stream is never larger: 11 bits per slot + 8 per escape
     assert len(oracle.compress(x, oracle.lut_from_histogram(hist))) <= len(oracle.compress(x, oracle.lut_from_sigma(sigma)))
+
+
+def test_data_lut_recovers_what_the_sigma_lut_misses():
+    """Two payloads the Gaussian rule fits badly.  ReLU output (half exact
+    zeros): the measured LUT takes exponent 0 first and codes almost every
+    value, where the sigma LUT escapes every zero.  A bucket of two layers
+    with different scales: no single sigma fits both."""
+    x = workloads.gaussian(1 << 20, 1.0, seed=3).copy()
+    x[(x & 0x8000) != 0] = 0
+    h = oracle.exponent_histogram(x).astype(np.int64)
+    lut = oracle.lut_from_histogram(h)
+    assert lut[0] == 0 and h[0] == (x == 0).sum()
+    assert sum(h[e] for e in lut) >= 0.97 * x.size
+    assert sum(h[e] for e in oracle.lut_from_sigma(1.0)) < 0.5 * x.size
+    mix = np.concatenate([workloads.gaussian(1 << 19, 0.02, seed=4), workloads.gaussian(1 << 19, 1e-3, seed=5)])
+    hm = oracle.exponent_histogram(mix).astype(np.int64)
+    rms = float(np.sqrt((0.02 ** 2 + 1e-3 ** 2) / 2))
+    assert sum(hm[e] for e in oracle.lut_from_histogram(hm)) > sum(hm[e] for e in oracle.lut_from_sigma(rms))
