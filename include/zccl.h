@@ -109,8 +109,9 @@ zccl_status_t zccl_lut_from_sigma(double sigma, zccl_lut_t* lut);
 uint64_t zccl_max_compressed_bytes(uint64_t n);
 
 /* Byte offset of the zero-point array in a stream of n elements; it depends
- * on n only, so header + chunk blocks of a stream have a size known before
- * compression.  Host only. */
+ * on n only, so header + chunk blocks of a stream (its frame) have a size
+ * known before compression, and only the zero-point tail varies with the
+ * data (see zccl_decompress_split).  Host only. */
 uint64_t zccl_zero_point_offset(uint64_t n);
 
 /* Workspace bytes for one call of `op`.  n: elements (compress, decompress,
@@ -141,6 +142,20 @@ zccl_status_t zccl_compress(const uint16_t* d_in, uint64_t n, const zccl_lut_t* 
 zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n,
                               void* d_ws, uint64_t ws_bytes, uint32_t* d_status,
                               cudaStream_t stream);
+
+/* Decompress a stream held in two pieces (ZipCCL 2.D: the static part of a
+ * two-phase all-to-all is sent first, and with the framing of 2.C its size is
+ * fixed): d_frame = the stream's first zccl_zero_point_offset(n) bytes (header
+ * and chunk blocks; their size depends on n only, so a receive of exactly
+ * that size can be posted before compression), d_tail = the rest, the
+ * zero-point array, tail_bytes long (the header's escape count rounded up to
+ * 128; d_tail may be NULL when tail_bytes == 0).  Both 16-byte aligned.  The
+ * result, checks and status are those of zccl_decompress on the two pieces
+ * joined; nothing is copied to join them.  The paper sends the parts; this
+ * receiving side is this library's. */
+zccl_status_t zccl_decompress_split(const void* d_frame, const void* d_tail, uint64_t tail_bytes, uint16_t* d_out,
+                                    uint64_t n, void* d_ws, uint64_t ws_bytes, uint32_t* d_status,
+                                    cudaStream_t stream);
 
 /* Batched compress of ragged segments in one launch (ZipCCL 2.D: the
  * static and dynamic parts of an MoE all-to-all payload).  d_segs is a

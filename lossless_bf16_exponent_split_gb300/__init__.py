@@ -47,6 +47,9 @@ _SIGS = {
     "zccl_decompress": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
                          ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p],
                         ctypes.c_int),
+    "zccl_decompress_split": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                               ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                               ctypes.c_void_p], ctypes.c_int),
     "zccl_compress_batched": ([ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                ctypes.c_void_p], ctypes.c_int),
@@ -136,6 +139,12 @@ def zccl_compress(d_in, n, lut, d_out, out_capacity, d_out_bytes, d_ws, ws_bytes
 
 def zccl_decompress(d_in, in_bytes, d_out, n, d_ws, ws_bytes, d_status, stream) -> int:
     return lib().zccl_decompress(d_in, in_bytes, d_out, n, d_ws, ws_bytes, d_status, stream)
+
+
+def zccl_decompress_split(d_frame, d_tail, tail_bytes, d_out, n, d_ws, ws_bytes, d_status, stream) -> int:
+    """zccl_decompress of a stream held as its fixed-size frame (the first
+    zccl_zero_point_offset(n) bytes) and its zero-point tail, apart."""
+    return lib().zccl_decompress_split(d_frame, d_tail, tail_bytes, d_out, n, d_ws, ws_bytes, d_status, stream)
 
 
 def zccl_compress_batched(d_segs, n_segs, total_n, lut, d_out_bytes, d_ws, ws_bytes, d_status,

@@ -12,7 +12,8 @@ import torch
 
 from . import (OP_COMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS, OP_DECOMPRESS_REDUCE, OK,
                ZcclError, check, zccl_compress, zccl_compress_batched, zccl_decompress,
-               zccl_decompress_reduce, zccl_decompress_reduce_local, zccl_exponent_histogram,
+               zccl_decompress_reduce, zccl_decompress_reduce_local, zccl_decompress_split,
+               zccl_exponent_histogram,
                zccl_lut_from_histogram, zccl_max_compressed_bytes, zccl_workspace_bytes)
 
 SEGMENT_DTYPE = np.dtype([("in", "<u8"), ("n", "<u8"), ("out", "<u8"), ("cap", "<u8")])
@@ -79,6 +80,18 @@ class Codec:
         check(zccl_decompress(stream_buf.data_ptr(), in_bytes, out.data_ptr() if n else 0, n, ws,
                               wsb, self.status.data_ptr(), _stream_handle(self.stream)),
               "zccl_decompress")
+        return out
+
+    def decompress_split(self, frame: torch.Tensor, tail: torch.Tensor | None, tail_bytes: int, n: int,
+                         out: torch.Tensor | None = None):
+        """Decompress a stream held as its frame (header + blocks, exactly
+        zccl_zero_point_offset(n) bytes) and its zero-point tail, apart."""
+        if out is None:
+            out = torch.empty(max(n, 1), dtype=torch.int16, device=self.device)[:n]
+        ws, wsb = self.workspace(zccl_workspace_bytes(OP_DECOMPRESS, n))
+        check(zccl_decompress_split(frame.data_ptr(), tail.data_ptr() if tail is not None and tail_bytes else 0,
+                                    tail_bytes, out.data_ptr() if n else 0, n, ws, wsb, self.status.data_ptr(),
+                                    _stream_handle(self.stream)), "zccl_decompress_split")
         return out
 
     def segment_table(self, segments) -> torch.Tensor:

@@ -272,11 +272,10 @@ __device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm
     uint32_t zbytes = 0, delta = 0, zc = 0;
     if (o0 + cnt <= sm.n_esc && cnt <= valid) {
         zc = cnt;
-        if (cnt) {
-            const uint64_t zp = zp_offset_of(a.n);
-            const uint64_t lo = zp + o0, lo16 = lo & ~15ull, hi16 = round_up(zp + o0 + cnt, 16);
+        if (cnt) {  // a.zp is 16-byte aligned: align the run's offsets within it
+            const uint64_t lo16 = o0 & ~15ull, hi16 = round_up(o0 + cnt, 16);
             zbytes = (uint32_t)(hi16 - lo16);
-            delta = (uint32_t)(lo - lo16);
+            delta = (uint32_t)(o0 - lo16);
         }
     } else {
         report(a.status, ZCCL_ERR_CORRUPT_STREAM);
@@ -284,7 +283,7 @@ __device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm
     sm.zdelta[buf] = delta;
     sm.zcount[buf] = zc;
     mbar_arrive_expect_tx(&sm.bar[buf], zbytes);
-    if (zbytes) bulk_g2s(sm.zpb[buf], a.in + ((zp_offset_of(a.n) + o0) & ~15ull), zbytes, &sm.bar[buf]);
+    if (zbytes) bulk_g2s(sm.zpb[buf], a.zp + (o0 & ~15ull), zbytes, &sm.bar[buf]);
 }
 
 __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const DecompressArgs a)

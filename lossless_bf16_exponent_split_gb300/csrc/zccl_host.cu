@@ -125,6 +125,35 @@ uint32_t grid_for(uint64_t units, int per_sm, int sms)
     return (uint32_t)std::max<uint64_t>(g, 1);
 }
 
+// zccl_decompress and zccl_decompress_split: the frame (header + blocks) at
+// `frame`, the zero-point array at `zp`, in_bytes = zp_offset + the bytes at zp.
+zccl_status_t decompress_impl(const uint8_t* frame, const uint8_t* zp, uint64_t in_bytes, uint16_t* d_out,
+                              uint64_t n, void* d_ws, uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream)
+{
+    if ((n > 0 && (d_out == nullptr || !aligned(d_out, 16))) || d_ws == nullptr || !aligned(d_ws, 16) ||
+        !aligned(d_status, 4))
+        return ZCCL_ERR_INVALID_ARG;
+    const uint64_t units = units_of(n);
+    const DecompressLayout l = decompress_layout(units);
+    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo* dev = device_info();
+    if (dev == nullptr) return ZCCL_ERR_CUDA;
+
+    DecompressArgs a{};
+    a.in = frame;
+    a.zp = zp;
+    a.in_bytes = in_bytes;
+    a.out = d_out;
+    a.n = n;
+    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
+    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
+    a.entry = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.entry);
+    a.status = d_status;
+    return launch_decompress(a, grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -244,28 +273,22 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
 zccl_status_t zccl_decompress(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n, void* d_ws,
                               uint64_t ws_bytes, uint32_t* d_status, cudaStream_t stream)
 {
-    if (n >= kMaxElems || d_in == nullptr || !aligned(d_in, 16) || (n > 0 && (d_out == nullptr || !aligned(d_out, 16))) ||
-        d_ws == nullptr || !aligned(d_ws, 16) || !aligned(d_status, 4))
+    if (n >= kMaxElems || d_in == nullptr || !aligned(d_in, 16) || in_bytes < zp_offset_of(n))
         return ZCCL_ERR_INVALID_ARG;
-    if (in_bytes < zp_offset_of(n)) return ZCCL_ERR_INVALID_ARG;
-    const uint64_t units = units_of(n);
-    const DecompressLayout l = decompress_layout(units);
-    if (ws_bytes < l.total) return ZCCL_ERR_BUFFER_TOO_SMALL;
-    const DeviceInfo* dev = device_info();
-    if (dev == nullptr) return ZCCL_ERR_CUDA;
+    return decompress_impl(reinterpret_cast<const uint8_t*>(d_in),
+                           reinterpret_cast<const uint8_t*>(d_in) + zp_offset_of(n), in_bytes, d_out, n, d_ws,
+                           ws_bytes, d_status, stream);
+}
 
-    DecompressArgs a{};
-    a.in = reinterpret_cast<const uint8_t*>(d_in);
-    a.in_bytes = in_bytes;
-    a.out = d_out;
-    a.n = n;
-    a.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    a.flags = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + kCtrlBytes);
-    a.entry = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.entry);
-    a.status = d_status;
-    return launch_decompress(a, grid_for(units, dev->decompress_per_sm, dev->sms), stream) == cudaSuccess
-               ? ZCCL_OK
-               : ZCCL_ERR_CUDA;
+zccl_status_t zccl_decompress_split(const void* d_frame, const void* d_tail, uint64_t tail_bytes, uint16_t* d_out,
+                                    uint64_t n, void* d_ws, uint64_t ws_bytes, uint32_t* d_status,
+                                    cudaStream_t stream)
+{
+    if (n >= kMaxElems || d_frame == nullptr || !aligned(d_frame, 16) || tail_bytes >= kMaxElems * 4 ||
+        (tail_bytes > 0 && (d_tail == nullptr || !aligned(d_tail, 16))))
+        return ZCCL_ERR_INVALID_ARG;
+    return decompress_impl(reinterpret_cast<const uint8_t*>(d_frame), reinterpret_cast<const uint8_t*>(d_tail),
+                           zp_offset_of(n) + tail_bytes, d_out, n, d_ws, ws_bytes, d_status, stream);
 }
 
 }  // extern "C"

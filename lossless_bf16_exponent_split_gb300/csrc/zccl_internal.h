@@ -45,8 +45,9 @@ struct ScanArgs {
 };
 
 struct DecompressArgs {
-    const uint8_t* in;
-    uint64_t in_bytes;
+    const uint8_t* in;           // header and chunk blocks (the frame)
+    const uint8_t* zp;           // the zero-point array: in + zp_offset, or a separate tail buffer
+    uint64_t in_bytes;           // zp_offset + the bytes available at zp
     uint16_t* out;
     uint64_t n;
     WsCtrl* ctrl;

@@ -84,6 +84,10 @@ def test_argument_errors_need_no_gpu(z):
     assert z.zccl_compress(**dict(ok, out_capacity=100)) == z.BUFFER_TOO_SMALL
     assert z.zccl_compress(**dict(ok, ws_bytes=64)) == z.BUFFER_TOO_SMALL
     assert z.zccl_decompress(A, 64, A, 4096, A, 1 << 16, 0, None) == z.INVALID_ARG  # in_bytes too small
+    assert z.zccl_decompress_split(A + 8, A, 128, A, 4096, A, 1 << 16, 0, None) == z.INVALID_ARG  # frame
+    assert z.zccl_decompress_split(A, A + 4, 128, A, 4096, A, 1 << 16, 0, None) == z.INVALID_ARG  # tail
+    assert z.zccl_decompress_split(A, 0, 128, A, 4096, A, 1 << 16, 0, None) == z.INVALID_ARG  # no tail
+    assert z.zccl_decompress_split(A, A, 128, A, 4096, A, 64, 0, None) == z.BUFFER_TOO_SMALL
     assert z.zccl_decompress_reduce(A, A, 0, A, 100, A, 1 << 16, 0, None) == z.INVALID_ARG
     wsr = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, 100, 4)
     assert z.zccl_decompress_reduce_local(A, A, 4, A, 4, 0, A, 100, A, wsr, 0, None) == z.INVALID_ARG  # local_pos >= S

@@ -259,3 +259,38 @@ def test_long_runs_full_parity(codec):
     torch.cuda.synchronize()
     assert codec.read_status() == 0
     assert torch.equal(y, xd)
+
+
+@pytest.mark.parametrize("n", [0, 1, 1025, 4096, 3 * 4096 + 5, 100_003])
+@pytest.mark.parametrize("kind", ["gauss", "special", "no_escape"])
+def test_decompress_split_frame_and_tail(codec, n, kind):
+    """The stream received as two separate buffers: its frame (header and
+    blocks, a size fixed by n) and its zero-point tail."""
+    x = {"gauss": lambda: workloads.gaussian(n, 0.02, seed=n + 1),
+         "special": lambda: workloads.special_values(n, seed=n + 2),
+         "no_escape": lambda: np.full(n, 0x3C00, np.uint16)}[kind]()
+    lut = LUTS["sigma0.02"]
+    stream = oracle.compress(x, lut)
+    zp = oracle.zero_point_offset(n)
+    frame = dev_bytes(stream[:zp])
+    tail_b = stream[zp:]
+    tail = dev_bytes(tail_b) if tail_b else None
+    if kind == "no_escape":
+        assert not tail_b
+    codec.reset_status()
+    y = codec.decompress_split(frame, tail, len(tail_b), n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 0
+    assert np.array_equal(host_u16(y), x)
+
+
+def test_decompress_split_short_tail_is_corrupt(codec):
+    n = 2 * 4096 + 3
+    x = workloads.special_values(n, seed=9)
+    stream = oracle.compress(x, LUTS["sigma0.02"])
+    zp = oracle.zero_point_offset(n)
+    assert len(stream) - zp >= 256
+    codec.reset_status()
+    codec.decompress_split(dev_bytes(stream[:zp]), dev_bytes(stream[zp:-128]), len(stream) - zp - 128, n)
+    torch.cuda.synchronize()
+    assert codec.read_status() == 3  # CORRUPT_STREAM
