@@ -259,6 +259,43 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
 zccl_status_t zccl_decompress_noalloc(const void* d_in, uint64_t in_bytes, uint16_t* d_out, uint64_t n,
                                       uint32_t* d_status, cudaStream_t stream);
 
+/* Reduce-scatter switcher (ZipCCL 2.D: profile the link's bandwidth and
+ * latency and the compression ratio, then run either the native
+ * reduce-scatter or a zipped all-to-all plus a local decompress-and-reduce,
+ * whichever is faster).  The pages give the inputs but no formula; this is
+ * a time model of the two paths, host only, with no collective:
+ *   ranks P, each holding `bytes` of BF16 (P shards of s = bytes / P);
+ *   native ring:  (P-1) * (latency + s / link)
+ *   zipped:       compress (P-1)*s  + (P-1) * (latency + ratio*s / link)
+ *                 + decompress-reduce P*s (the own shard uncompressed)
+ * where a codec step on x bytes of BF16 input takes fixed_us + x / gbs.
+ * Rates are GB/s (1e9 bytes/s) of BF16 input, e.g. measured with this
+ * library on the payload; ratio = compressed bytes / BF16 bytes. */
+typedef struct {
+    uint32_t ranks;           /* P >= 1                                      */
+    uint64_t bytes;           /* BF16 bytes per rank (all P shards)          */
+    double ratio;             /* finite, > 0                                 */
+    double link_gbs;          /* per-rank link bandwidth, finite, > 0       */
+    double link_latency_us;   /* per message, finite, >= 0                  */
+    double compress_gbs;      /* finite, > 0                                 */
+    double compress_fixed_us; /* per call, finite, >= 0                      */
+    double reduce_gbs;        /* decompress-reduce, finite, > 0             */
+    double reduce_fixed_us;   /* per call, finite, >= 0                      */
+} zccl_rs_model_t;
+
+typedef struct {
+    int zipped;                 /* 1: zipped all-to-all + local reduce is faster */
+    double native_us;           /* modelled time of each path                    */
+    double zipped_us;
+    double breakeven_link_gbs;  /* zipped wins below this link bandwidth; 0 if
+                                   ratio >= 1 (never), independent of latency */
+} zccl_rs_plan_t;
+
+/* Fill *plan from *model (ties go to the native path; P == 1 exchanges
+ * nothing: native, all times 0).  INVALID_ARG on a null pointer or a field
+ * outside its range.  Host only. */
+zccl_status_t zccl_rs_plan(const zccl_rs_model_t* model, zccl_rs_plan_t* plan);
+
 /* Static text for a status code. */
 const char* zccl_status_string(zccl_status_t status);
 

@@ -68,8 +68,23 @@ _SIGS = {
     "zccl_lut_from_histogram": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_lut_from_data": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
                            ctypes.c_int),
+    "zccl_rs_plan": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_status_string": ([ctypes.c_int], ctypes.c_char_p),
 }
+
+
+class RsModel(ctypes.Structure):
+    """zccl_rs_model_t"""
+    _fields_ = [("ranks", ctypes.c_uint32), ("bytes", ctypes.c_uint64), ("ratio", ctypes.c_double),
+                ("link_gbs", ctypes.c_double), ("link_latency_us", ctypes.c_double),
+                ("compress_gbs", ctypes.c_double), ("compress_fixed_us", ctypes.c_double),
+                ("reduce_gbs", ctypes.c_double), ("reduce_fixed_us", ctypes.c_double)]
+
+
+class RsPlan(ctypes.Structure):
+    """zccl_rs_plan_t"""
+    _fields_ = [("zipped", ctypes.c_int), ("native_us", ctypes.c_double), ("zipped_us", ctypes.c_double),
+                ("breakeven_link_gbs", ctypes.c_double)]
 
 
 class ZcclError(RuntimeError):
@@ -201,6 +216,17 @@ def zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream) -> int:
 
 def zccl_check_bounded_wait(limit_us, d_status, stream) -> int:
     return lib().zccl_check_bounded_wait(limit_us, d_status, stream)
+
+
+def zccl_rs_plan(ranks, nbytes, ratio, link_gbs, link_latency_us, compress_gbs, compress_fixed_us,
+                 reduce_gbs, reduce_fixed_us) -> dict:
+    """The switcher's choice and both paths' modelled times (host only)."""
+    m = RsModel(ranks, nbytes, ratio, link_gbs, link_latency_us, compress_gbs, compress_fixed_us, reduce_gbs,
+                reduce_fixed_us)
+    p = RsPlan()
+    check(lib().zccl_rs_plan(ctypes.addressof(m), ctypes.addressof(p)), "zccl_rs_plan")
+    return {"zipped": bool(p.zipped), "native_us": p.native_us, "zipped_us": p.zipped_us,
+            "breakeven_link_gbs": p.breakeven_link_gbs}
 
 
 def zccl_status_string(status: int) -> str:
