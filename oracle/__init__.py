@@ -1,7 +1,9 @@
 """Oracle for the lossless BF16 exponent codec -- TEST INFRASTRUCTURE ONLY.
 
 The oracle is the plain C file ``zccl_oracle.c`` beside this module, compiled
-with gcc into ``oracle/_build/libzccl_oracle.so`` and called through ctypes.
+with gcc into ``oracle/_build/libzccl_oracle.so`` and called through ctypes,
+plus ``switcher.py``, the reduce-scatter switcher's time model in plain
+Python (fp64).
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (the CUDA library and its
 Python binding) never imports it and shares no code with it.
