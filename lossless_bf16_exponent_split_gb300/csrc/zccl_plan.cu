@@ -9,7 +9,7 @@
 #include <cmath>
 #include <cstdint>
 
-#include "zccl.h"
+#include "../../include/zccl.h"
 
 namespace {
 
