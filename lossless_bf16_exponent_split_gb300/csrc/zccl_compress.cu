@@ -162,20 +162,24 @@ __device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t 
 
 // Codes one chunk (already in sm.in[buf]) into sm.blk, stores the block and
 // stages the escapes; returns the chunk's escape count (all threads).
+// kFull: a whole 4096-element chunk (every chunk but a segment's last), so
+// the block and plane offsets are constants and no lane masks its tail.
+template <bool kFull>
 __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSmem& sm, int buf, uint32_t c,
-                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid,
+                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid_arg,
                                                bool timed_out)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t L = slots_of(valid);
+    const uint32_t valid = kFull ? kChunk : valid_arg;
+    const uint32_t L = kFull ? kChunk : slots_of(valid);
     const uint8_t* src = sm.in[buf];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-        if (e0 >= L) continue;
+        if (!kFull && e0 >= L) continue;
         uint4 v = *reinterpret_cast<const uint4*>(src + 2 * e0);
         uint32_t keep = 0xFFu;
-        if (e0 + 8 > valid) {
+        if (!kFull && e0 + 8 > valid) {
             const uint32_t nv = valid > e0 ? valid - e0 : 0;  // 0..7
             keep = (1u << nv) - 1u;
             const uint32_t m0 = (keep & 1 ? 0x0000FFFFu : 0u) | (keep & 2 ? 0xFFFF0000u : 0u);
@@ -190,16 +194,17 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
         const uint32_t smA = (hi01 & 0x80808080u) | (lo01 & 0x7F7F7F7Fu);
         const uint32_t smB = (hi23 & 0x80808080u) | (lo23 & 0x7F7F7F7Fu);
         *reinterpret_cast<uint2*>(sm.blk + e0) = make_uint2(smA, smB);
-        // code bits: byte p of acc = plane p bits of the 8 elements
+        // code bits: byte p of acc = plane p bits of the 8 elements (the
+        // shifted table words share no bit, so adding them is OR'ing them)
         uint32_t acc = sm.code_bits[(v.x >> 7) & 0xFF];
-        acc |= sm.code_bits[(v.x >> 23) & 0xFF] << 1;
-        acc |= sm.code_bits[(v.y >> 7) & 0xFF] << 2;
-        acc |= sm.code_bits[(v.y >> 23) & 0xFF] << 3;
-        acc |= sm.code_bits[(v.z >> 7) & 0xFF] << 4;
-        acc |= sm.code_bits[(v.z >> 23) & 0xFF] << 5;
-        acc |= sm.code_bits[(v.w >> 7) & 0xFF] << 6;
-        acc |= sm.code_bits[(v.w >> 23) & 0xFF] << 7;
-        acc &= keep * 0x010101u;
+        acc += sm.code_bits[(v.x >> 23) & 0xFF] << 1;
+        acc += sm.code_bits[(v.y >> 7) & 0xFF] << 2;
+        acc += sm.code_bits[(v.y >> 23) & 0xFF] << 3;
+        acc += sm.code_bits[(v.z >> 7) & 0xFF] << 4;
+        acc += sm.code_bits[(v.z >> 23) & 0xFF] << 5;
+        acc += sm.code_bits[(v.w >> 7) & 0xFF] << 6;
+        acc += sm.code_bits[(v.w >> 23) & 0xFF] << 7;
+        if (!kFull) acc &= keep * 0x010101u;
         uint8_t* planes = sm.blk + L + (e0 >> 3);
         planes[0] = (uint8_t)acc;
         planes[L / 8] = (uint8_t)(acc >> 8);
@@ -215,10 +220,11 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
     }
     // escapes: words from the planes, chunk-local compaction into the stage
     uint32_t esc = 0;
-    if (tid < (int)(L / 32)) {
+    if (kFull || tid < (int)(L / 32)) {
         const uint32_t* pw = reinterpret_cast<const uint32_t*>(sm.blk + L);
         const uint32_t w0 = 32u * tid;
-        const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+        const uint32_t vmask =
+            kFull || w0 + 32 <= valid ? 0xFFFFFFFFu : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
         esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
     }
     uint32_t agg;
@@ -319,7 +325,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
                 reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
             __syncthreads();
         }
-        const uint32_t agg = code_chunk(a, sm, buf, c, d, cl, valid, timed_out);
+        const uint32_t agg = valid == kChunk ? code_chunk<true>(a, sm, buf, c, d, cl, valid, timed_out)
+                                             : code_chunk<false>(a, sm, buf, c, d, cl, valid, timed_out);
         if (agg == kAborted) {  // a bulk load never landed (bounded wait ran out)
             if (tid == 0) {
                 sm.abort = 1;
