@@ -286,6 +286,59 @@ __device__ __forceinline__ void start_zp(const DecompressArgs& a, DecodeSmem& sm
     if (zbytes) bulk_g2s(sm.zpb[buf], a.zp + (o0 & ~15ull), zbytes, &sm.bar[buf]);
 }
 
+// Phase 2 of one chunk whose block and zero-point run are in buffer buf:
+// escaped exponents to their slots, then 8 elements a thread rebuilt and
+// stored.  kFull: a whole 4096-element chunk (every chunk but the last), so
+// the plane offsets are constants and no store is partial.
+template <bool kFull>
+__device__ __forceinline__ void decode_chunk(const DecompressArgs& a, DecodeSmem& sm, int buf, uint64_t first,
+                                             uint32_t valid_arg, uint32_t lut_lo, uint32_t lut_hi)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t valid = kFull ? kChunk : valid_arg;
+    const uint32_t L = kFull ? kChunk : slots_of(valid);
+    const uint8_t* blk = sm.blk[buf];
+    uint32_t esc = 0;
+    if (kFull || tid < (int)(L / 32)) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+        const uint32_t w0 = 32u * tid;
+        const uint32_t vmask =
+            kFull || w0 + 32 <= valid ? 0xFFFFFFFFu : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+        esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
+    }
+    uint32_t agg;
+    const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
+    const bool good = agg == sm.zcount[buf];
+    if (good) {
+        const uint8_t* src = sm.zpb[buf] + sm.zdelta[buf] + excl;
+        uint32_t m = esc, j = 0;
+        while (m) {
+            const uint32_t bb = __ffs(m) - 1;
+            m &= m - 1;
+            sm.expo[32u * tid + bb] = src[j++];
+        }
+    } else if (tid == 0) {
+        report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+    }
+    __syncthreads();
+    if (good) {
+        uint16_t* dst = a.out + first;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
+            if (!kFull && e0 >= valid) continue;
+            const uint4 o = decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
+                                    blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
+                                    *reinterpret_cast<const uint2*>(sm.expo + e0));
+            if (kFull || e0 + 8 <= valid) {
+                *reinterpret_cast<uint4*>(dst + e0) = o;
+            } else {
+                store_partial(dst + e0, o, valid - e0);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const DecompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -480,7 +533,6 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
         if (c >= T) break;
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
-        const uint32_t L = slots_of(valid);
         if (!mbar_wait(&sm.bar[buf], (k >> 1) & 1)) atomicExch(&sm.abort, 1u);
         __syncthreads();
         if (sm.abort) {
@@ -491,46 +543,10 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             break;
         }
         if (tid == 0 && tn < T) en = ld_relaxed_u64(a.entry + tn);  // used at the refill below
-        const uint8_t* blk = sm.blk[buf];
-        uint32_t esc = 0;
-        if (tid < (int)(L / 32)) {
-            const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-            const uint32_t w0 = 32u * tid;
-            const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
-                                   : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-            esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
-        }
-        uint32_t agg;
-        const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
-        const bool good = agg == sm.zcount[buf];
-        if (good) {
-            const uint8_t* src = sm.zpb[buf] + sm.zdelta[buf] + excl;
-            uint32_t m = esc, j = 0;
-            while (m) {
-                const uint32_t bb = __ffs(m) - 1;
-                m &= m - 1;
-                sm.expo[32u * tid + bb] = src[j++];
-            }
-        } else if (tid == 0) {
-            report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-        }
-        __syncthreads();
-        if (good) {
-            uint16_t* dst = a.out + first;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-                if (e0 >= valid) continue;
-                const uint4 o = decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
-                                        blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
-                                        *reinterpret_cast<const uint2*>(sm.expo + e0));
-                if (e0 + 8 <= valid) {
-                    *reinterpret_cast<uint4*>(dst + e0) = o;
-                } else {
-                    store_partial(dst + e0, o, valid - e0);
-                }
-            }
-        }
+        if (valid == kChunk)
+            decode_chunk<true>(a, sm, buf, first, valid, lut_lo, lut_hi);
+        else
+            decode_chunk<false>(a, sm, buf, first, valid, lut_lo, lut_hi);
         __syncthreads();  // buffer buf (block, zero-point run, expo) is free again
         if (tid == 0) {
             uint32_t t = tn;
@@ -551,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
                 tn = T;
             }
         }
-        __syncthreads();
+        // (no barrier: what thread 0 just wrote for buffer buf is read two
+        // iterations on, after the next iteration's barriers)
     }
     if (tid == 0) call_end(a.ctrl, calls, sm.hdr_ok && published == G - 1);
 }
