@@ -320,7 +320,9 @@ __device__ __forceinline__ void decode_chunk(const DecompressArgs& a, DecodeSmem
     } else if (tid == 0) {
         report(a.status, ZCCL_ERR_CORRUPT_STREAM);
     }
-    __syncthreads();
+    // warp w decodes elements [1024w, 1024w + 1024): the escape words of its
+    // own lanes, so its exponents in sm.expo were placed by the warp itself
+    __syncwarp();
     if (good) {
         uint16_t* dst = a.out + first;
 #pragma unroll

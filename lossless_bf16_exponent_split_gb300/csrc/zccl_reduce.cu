@@ -175,10 +175,6 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
     for (;; ++j) {
         if (c >= total) break;
         const int st = j % kStages;
-        if (tid == 0) {
-            issue_step(a, sm, t, j + kStages - 1, total, ahead);
-            ahead = load_offsets(a, j + kStages, total);
-        }
         uint32_t s = 0;
         const uint32_t kind = step_kind(a, q, &s);
         const uint64_t first = (uint64_t)c * kChunk;
@@ -197,6 +193,13 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         if (sm.abort) {
             if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
             break;
+        }
+        // every thread is past step j - 1, so its stage is free: refill it
+        // with step j + kStages - 1 (this barrier is also the previous
+        // step's end)
+        if (tid == 0) {
+            issue_step(a, sm, t, j + kStages - 1, total, ahead);
+            ahead = load_offsets(a, j + kStages, total);
         }
         if (kind == kStepStream) {
             uint32_t esc = 0;
@@ -220,7 +223,9 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             } else if (tid == 0) {
                 report(a.status, ZCCL_ERR_CORRUPT_STREAM);
             }
-            __syncthreads();
+            // warp w folds elements [1024w, 1024w + 1024): its own lanes'
+            // escape words, so the warp placed its exponents itself
+            __syncwarp();
         }
         const uint32_t lut_lo = t.lut[2 * s], lut_hi = t.lut[2 * s + 1];
 #pragma unroll
@@ -264,15 +269,16 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
                 }
             }
         }
-        __syncthreads();
         if (++q == Q) {  // the next chunk's first step
             q = 0;
             c += gridDim.x;
         }
     }
-    // steps still in flight after an early stop: wait for them (bounded)
+    // steps still in flight after an early stop at step j: j + 1 .. j + kStages - 2
+    // (step j + kStages - 1 is issued only after step j's first barrier); wait for
+    // them (bounded)
     if (tid == 0 && sm.abort) {
-        for (uint32_t jj = j + 1; jj < j + kStages; ++jj) {
+        for (uint32_t jj = j + 1; jj + 1 < j + kStages; ++jj) {
             if (blockIdx.x + (jj / Q) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
         }
     }
