@@ -102,8 +102,74 @@ def ncu_traffic(kernel: str, workload: str):
     return float(m.group(1))
 
 
+class NvmlClockPoller:
+    """SM clock and clock-event reasons read through NVML (ctypes) every
+    ~0.5 ms from a background thread, so that a timed region of a few
+    milliseconds still gets samples.  Read-only; any NVML failure leaves it
+    inactive."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device_index: int):
+        import ctypes
+        import threading
+        self.samples, self.max_mhz, self.reasons = [], None, set()
+        self.stop = threading.Event()
+        self.thread = None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            self.nvml = nvml
+            self.handle = ctypes.c_void_p()
+            found = False
+            try:  # by UUID: NVML may number the GPUs differently from CUDA
+                import torch
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                found = nvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(self.handle)) == 0
+            except Exception:
+                found = False
+            if not found and nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index),
+                                                                 ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            if nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+                self.max_mhz = float(mx.value)
+            get_reasons = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.get_reasons = get_reasons
+            self.thread = threading.Thread(target=self._run, daemon=True)
+        except Exception:
+            self.thread = None
+
+    def _run(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self.stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if self.get_reasons(self.handle, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.0005)
+
+    def __enter__(self):
+        if self.thread is not None:
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons during the timed region."""
+    """Clocks and throttle reasons during the timed region: NVML polled every
+    ~0.5 ms inside it (see NvmlClockPoller), and nvidia-smi every 100 ms from
+    0.3 s before to 0.2 s after it as a fallback."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -113,6 +179,7 @@ class ClockSampler:
         self.idx = device_index
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.poller = None
 
     def __enter__(self):
         try:
@@ -124,9 +191,12 @@ class ClockSampler:
             time.sleep(0.3)
         except Exception:
             self.proc = None
+        self.poller = NvmlClockPoller(self.idx).__enter__()
         return self
 
     def __exit__(self, *exc):
+        if self.poller is not None:
+            self.poller.__exit__(*exc)
         if self.proc is not None:
             time.sleep(0.2)
             self.proc.terminate()
@@ -137,6 +207,10 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        p = self.poller
+        if p is not None and p.samples:
+            return {"sm_mhz": statistics.median(p.samples), "sm_max_mhz": p.max_mhz, "samples": len(p.samples),
+                    "reasons": sorted(p.reasons), "source": "nvml, polled during the timed region"}
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, mx, reasons = [], [], set()
@@ -156,7 +230,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons), "source": "nvidia-smi, 100 ms around the timed region"}
 
 
 # ---------------------------------------------------------------------------
