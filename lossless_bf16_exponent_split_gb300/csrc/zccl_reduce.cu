@@ -75,11 +75,22 @@ __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t 
 // the plain BF16 of the rank's own shard at local_pos.
 enum : uint32_t { kStepStream = 0, kStepLocal = 1, kStepOut = 2 };
 
-__device__ __forceinline__ uint32_t steps_per_chunk(const ReduceArgs& a) { return a.S + (a.accumulate ? 1u : 0u); }
+// kPlain: some steps read plain BF16 (the rank's own shard, or the output
+// being accumulated into); without them every step is a stream, in order.
+template <bool kPlain>
+__device__ __forceinline__ uint32_t steps_per_chunk(const ReduceArgs& a)
+{
+    return kPlain ? a.S + (a.accumulate ? 1u : 0u) : a.S;
+}
 
 // Kind of step q of a chunk; *shard gets the input position of a stream step.
+template <bool kPlain>
 __device__ __forceinline__ uint32_t step_kind(const ReduceArgs& a, uint32_t q, uint32_t* shard)
 {
+    if (!kPlain) {
+        *shard = q;
+        return kStepStream;
+    }
     if (a.accumulate) {
         if (q == 0) return kStepOut;
         --q;
@@ -97,13 +108,14 @@ struct StepOffsets {
     uint32_t local, count;
 };
 
+template <bool kPlain>
 __device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t j, uint32_t total)
 {
     StepOffsets o{0, 0, 0};
-    const uint32_t Q = steps_per_chunk(a);
+    const uint32_t Q = steps_per_chunk<kPlain>(a);
     const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
     uint32_t s = 0;
-    if (c >= total || step_kind(a, j % Q, &s) != kStepStream) return o;
+    if (c >= total || step_kind<kPlain>(a, j % Q, &s) != kStepStream) return o;
     const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
     const uint64_t idx = (uint64_t)s * total + c;
     o.base = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks);
@@ -114,14 +126,15 @@ __device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_
 
 // Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / Q) * gridDim.x,
 // step j % Q) into stage j % kStages.
+template <bool kPlain>
 __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t j,
                                            uint32_t total, const StepOffsets& off)
 {
-    const uint32_t Q = steps_per_chunk(a);
+    const uint32_t Q = steps_per_chunk<kPlain>(a);
     const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
     if (c >= total) return;
     uint32_t s = 0;
-    const uint32_t kind = step_kind(a, j % Q, &s);
+    const uint32_t kind = step_kind<kPlain>(a, j % Q, &s);
     const int st = j % kStages;
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     if (kind != kStepStream) {  // plain BF16: whole 16-byte pieces by bulk copy, the rest by plain loads
@@ -156,15 +169,17 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
 // All threads of the CTA: the CTA's chunks (static stride), each over its
 // steps in order.  The fp32 sums are kept as pairs and added with the
 // two-lane add (each lane rounds to nearest even exactly as a scalar add).
+template <bool kPlain>
 __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t total = (uint32_t)units_of(a.n);
-    const uint32_t Q = steps_per_chunk(a);
+    const uint32_t Q = steps_per_chunk<kPlain>(a);
     StepOffsets ahead{0, 0, 0};  // thread 0: offsets of the next step to queue
     if (tid == 0) {
-        for (uint32_t j = 0; j + 1 < kStages; ++j) issue_step(a, sm, t, j, total, load_offsets(a, j, total));
-        ahead = load_offsets(a, kStages - 1, total);
+        for (uint32_t j = 0; j + 1 < kStages; ++j)
+            issue_step<kPlain>(a, sm, t, j, total, load_offsets<kPlain>(a, j, total));
+        ahead = load_offsets<kPlain>(a, kStages - 1, total);
     }
 
     float2 acc[16];
@@ -176,7 +191,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         if (c >= total) break;
         const int st = j % kStages;
         uint32_t s = 0;
-        const uint32_t kind = step_kind(a, q, &s);
+        const uint32_t kind = step_kind<kPlain>(a, q, &s);
         const uint64_t first = (uint64_t)c * kChunk;
         const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
         const uint32_t L = slots_of(valid);
@@ -198,8 +213,8 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         // with step j + kStages - 1 (this barrier is also the previous
         // step's end)
         if (tid == 0) {
-            issue_step(a, sm, t, j + kStages - 1, total, ahead);
-            ahead = load_offsets(a, j + kStages, total);
+            issue_step<kPlain>(a, sm, t, j + kStages - 1, total, ahead);
+            ahead = load_offsets<kPlain>(a, j + kStages, total);
         }
         if (kind == kStepStream) {
             uint32_t esc = 0;
@@ -284,6 +299,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
     }
 }
 
+template <bool kPlain>
 __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -326,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
     }
     pdl_wait();  // offsets of the scan kernel
     if (__syncthreads_and(ok)) {
-        reduce_chunks(a, sm, t);
+        reduce_chunks<kPlain>(a, sm, t);
     } else {  // a bad header: nothing to decode, but leave the scratch clear
         for (uint32_t c = blockIdx.x; c < total; c += gridDim.x)
             for (uint32_t s = tid; s < a.S; s += kThreads) {
@@ -350,22 +366,37 @@ cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_
                           cudaStream_t stream)
 {
     const size_t smem = reduce_smem_bytes(a.S);
-    cudaError_t e = cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const bool plain = a.local != nullptr || a.accumulate;
+    cudaError_t e = plain ? cudaFuncSetAttribute(reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem)
+                          : cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
     if (e != cudaSuccess) return e;
     e = launch_scan(s, grid_scan, stream);
     if (e != cudaSuccess) return e;
-    return launch_dependent(reduce_kernel, grid, kThreads, smem, stream, a);
+    return plain ? launch_dependent(reduce_kernel<true>, grid, kThreads, smem, stream, a)
+                 : launch_dependent(reduce_kernel<false>, grid, kThreads, smem, stream, a);
 }
 
-int reduce_ctas_per_sm(uint32_t S)
+template <bool kPlain>
+static int reduce_occupancy(size_t smem)
 {
     int blocks = 0;
-    const size_t smem = reduce_smem_bytes(S);
-    if (cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(reduce_kernel<kPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
         return 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, reduce_kernel, kThreads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, reduce_kernel<kPlain>, kThreads, smem) !=
+        cudaSuccess)
         return 1;
     return blocks > 0 ? blocks : 1;
+}
+
+// CTAs per SM for either instance (the grid is sized once for both)
+int reduce_ctas_per_sm(uint32_t S)
+{
+    const size_t smem = reduce_smem_bytes(S);
+    const int a = reduce_occupancy<true>(smem), b = reduce_occupancy<false>(smem);
+    return a < b ? a : b;
 }
 
 }  // namespace zccl
