@@ -28,10 +28,10 @@ __device__ __forceinline__ uint32_t spread_nibbles(uint32_t x)
 // their plane bytes (bit k = element k), lut_lo/lut_hi the 8-entry byte
 // table (entry 0 unused, entry c = exponent of code c), `xe` the escaped
 // exponents at the elements' slots.  Returns the 8 BF16 values.
-__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
-                                         uint32_t lut_hi, uint2 xe)
+// 8 elements from their code nibbles N (nibble k = element k's 3-bit code),
+// sign-mantissa bytes and escaped exponents.
+__device__ __forceinline__ uint4 decode8_nibbles(uint32_t N, uint2 smb, uint32_t lut_lo, uint32_t lut_hi, uint2 xe)
 {
-    const uint32_t N = spread_nibbles(pb0) | (spread_nibbles(pb1) << 1) | (spread_nibbles(pb2) << 2);
     uint32_t e_lo = __byte_perm(lut_lo, lut_hi, N);        // nibble k of N selects byte k
     uint32_t e_hi = __byte_perm(lut_lo, lut_hi, N >> 16);
     const uint32_t m_lo = __byte_perm(0xFFu, 0u, N);       // 0xFF where the code is 000
@@ -47,7 +47,22 @@ __device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, 
                       __byte_perm(lo_b, hi_b, 0x5140), __byte_perm(lo_b, hi_b, 0x7362));
 }
 
-// Stores the first `count` (< 8) of 8 packed BF16 values.
+__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
+                                         uint32_t lut_hi, uint2 xe)
+{
+    const uint32_t N = spread_nibbles(pb0) | (spread_nibbles(pb1) << 1) | (spread_nibbles(pb2) << 2);
+    return decode8_nibbles(N, smb, lut_lo, lut_hi, xe);
+}
+
+// The same with the bit spreading looked up: spread[b] = spread_nibbles(b),
+// a 256-word table in shared memory (three loads instead of ~18 ALU ops).
+__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
+                                         uint32_t lut_hi, uint2 xe, const uint32_t* spread)
+{
+    const uint32_t N = spread[pb0] | (spread[pb1] << 1) | (spread[pb2] << 2);
+    return decode8_nibbles(N, smb, lut_lo, lut_hi, xe);
+}
+
 __device__ __forceinline__ void store_partial(uint16_t* dst, uint4 o, uint32_t count)
 {
 #pragma unroll

@@ -51,6 +51,7 @@ struct __align__(16) ReduceSmem {
     uint32_t scan[kThreads / 32];
     uint32_t abort;
     uint32_t last;
+    uint32_t spread[256];  // spread_nibbles of every byte
 };
 // followed by per-shard tables: const uint8_t* base[S]; uint64_t n_esc[S]; uint32_t lut[S][2]
 
@@ -250,7 +251,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
                 const uint4 o = kind == kStepStream
                                     ? decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
                                               blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo,
-                                              lut_hi, *reinterpret_cast<const uint2*>(sm.expo + e0))
+                                              lut_hi, *reinterpret_cast<const uint2*>(sm.expo + e0), sm.spread)
                                     : *reinterpret_cast<const uint4*>(blk + 2 * e0);
                 const uint32_t w[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
         t.base[s] = base;
         ok = ok && good;
     }
+    for (uint32_t b = tid; b < 256; b += kThreads) sm.spread[b] = spread_nibbles(b);
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
         fence_mbar_init();
