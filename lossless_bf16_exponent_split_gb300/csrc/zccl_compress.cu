@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             break;
         }
         if (tid == kBookkeeper) {  // (thread 0 is busy with the tickets and the bulk copies)
-            a.counts[c] = agg;
+            a.counts[c] = agg + 1;  // (0: not written yet)
             // the chunk's escapes carry into the next run unless its segment
             // ends inside this run
             const uint32_t r = run_of(c, sh);
@@ -398,7 +398,30 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
 
     // ---- phase 2: run b.  carry = escapes from the start of lo's segment ----
     // Once every chunk is coded (thread 0 polls the call's counter), the
-    // escapes on the flag words of runs [h0, b) are the carry.
+    // escapes on the flag words of runs [h0, b) are the carry.  A run word is
+    // final once its count says the run is complete, and a chunk count once
+    // it is nonzero, so both are loaded before the wait; only what was not
+    // final yet is loaded again after it.  (The staged escape bytes are read
+    // only after the wait and its acquire fence.)
+    const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
+    const uint32_t h0 = st < lo ? run_of(st, sh) : b;  // flag words [h0, b) make the carry
+    uint64_t part = 0;
+    bool reload = false;  // some run word of mine was not final yet
+    for (uint32_t q0 = h0 + tid; q0 < b; q0 += 8 * kThreads) {  // all loads of a round in flight at once
+        uint64_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = q0 + j * kThreads < b ? __ldcg(acc + q0 + j * kThreads) : 0ull;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t q = q0 + j * kThreads;
+            if (q >= b) continue;
+            const uint64_t size = run_lo(q + 1, T, sh) - run_lo(q, T, sh);
+            if ((v[j] >> kDoneShift) == size) part += v[j] & (kDoneOne - 1);
+            else reload = true;
+        }
+    }
+    const uint32_t nb0 = min(kBatch, hi - lo);
+    uint32_t cnt0 = tid < (int)nb0 ? __ldcg(a.counts + lo + tid) : 1u;  // my chunk count + 1 (first batch)
     if (tid == 0) {
         const bool ok = wait_count(&a.ctrl->done[par], T + G);
         fence_acq_rel_gpu();  // what the coders wrote before counting themselves done
@@ -413,15 +436,15 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         if (tid == kBookkeeper) call_end(a.ctrl, sm.calls, last);
         return;
     }
-    const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
-    const uint32_t h0 = st < lo ? run_of(st, sh) : b;  // flag words [h0, b) make the carry
-    uint64_t part = 0;
-    for (uint32_t q0 = h0 + tid; q0 < b; q0 += 8 * kThreads) {  // all loads of a round in flight at once
-        uint64_t v[8];
+    if (reload) {  // every run is complete now: load my words again
+        part = 0;
+        for (uint32_t q0 = h0 + tid; q0 < b; q0 += 8 * kThreads) {
+            uint64_t v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = q0 + j * kThreads < b ? __ldcg(acc + q0 + j * kThreads) : 0ull;
+            for (int j = 0; j < 8; ++j) v[j] = q0 + j * kThreads < b ? __ldcg(acc + q0 + j * kThreads) : 0ull;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) part += v[j] & (kDoneOne - 1);
+            for (int j = 0; j < 8; ++j) part += v[j] & (kDoneOne - 1);
+        }
     }
     uint64_t carry = block_sum_u64<kThreads>(part, sm.scan64);
     uint32_t* stage32 = reinterpret_cast<uint32_t*>(a.stage);
@@ -430,7 +453,9 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         // issue every load of the batch before using any: my chunk count and
         // the first staged word of each of my warp's first 8 chunks
         const uint32_t cc = base + tid;
-        const uint32_t cnt = tid < (int)nb ? __ldcg(a.counts + cc) : 0u;
+        uint32_t cnt1 = base == lo ? cnt0 : (tid < (int)nb ? __ldcg(a.counts + cc) : 1u);
+        if (cnt1 == 0) cnt1 = __ldcg(a.counts + cc);  // written before the wait ended
+        const uint32_t cnt = tid < (int)nb ? cnt1 - 1 : 0u;
         uint32_t v[8];
 #pragma unroll
         for (int ii = 0; ii < 8; ++ii) {
