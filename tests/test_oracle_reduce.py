@@ -30,6 +30,36 @@ def test_rounding_matches_library_cast_on_random_patterns():
     assert np.array_equal(oracle.round_bf16_array(f), torch_bf16_bits(f))
 
 
+def _nearest_bf16_by_distance(u):
+    """The definition itself, for finite fp32 bit patterns u: of the two BF16
+    values around |x| (truncation and the next one up, the next up past the
+    largest finite being 2^128, i.e. infinity), the one at the smaller exact
+    distance (computed in double, where every difference of these values is
+    exact), ties to the even mantissa; the sign is kept."""
+    mag = u & np.uint32(0x7FFFFFFF)
+    lo = mag >> np.uint32(16)
+    hi = lo + np.uint32(1)
+    v = mag.view(np.float32).astype(np.float64)
+    vlo = (lo << np.uint32(16)).view(np.float32).astype(np.float64)
+    vhi = np.where(hi == 0x7F80, 2.0 ** 128, (hi << np.uint32(16)).view(np.float32).astype(np.float64))
+    dlo, dhi = v - vlo, vhi - v
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return (pick | ((u >> np.uint32(16)) & np.uint32(0x8000))).astype(np.uint16)
+
+
+def test_rounding_matches_exact_distance_on_1e8_patterns():
+    """10^8 random finite fp32 patterns against the exact-distance definition
+    (independent of the oracle's bit trick and of any library cast)."""
+    rng = np.random.default_rng(12)
+    total = 0
+    while total < 100_000_000:
+        u = rng.integers(0, 2 ** 32, size=10_000_000, dtype=np.uint64).astype(np.uint32)
+        u = u[(u & np.uint32(0x7F800000)) != np.uint32(0x7F800000)]  # finite only (NaN, Inf: hand cases)
+        got = oracle.round_bf16_array(u.view(np.float32))
+        assert np.array_equal(got, _nearest_bf16_by_distance(u))
+        total += u.size
+
+
 def test_rounding_near_every_bf16_midpoint():
     """For every BF16 magnitude b: the exact midpoint above it and its two fp32
     neighbours."""
