@@ -350,6 +350,51 @@ def cpu_baseline(name, budget_s=12.0):
             "sample": f"{op} of the first {n} elements of the workload's distribution, {reps} reps"}
 
 
+def _oracle_slice_worker(name, k, budget_s):
+    """One process of cpu_baseline_all_cores: slice k of the workload's
+    distribution, generated here, run through the oracle for budget_s."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    from lossless_bf16_exponent_split_gb300 import workloads as w
+    cfg = w.CONFIGS[name]
+    lut = oracle.lut_from_sigma(cfg["sigma"])
+    if name in ("rs_local", "rs_local_own"):
+        per = 1 << 18
+        streams = [oracle.compress(x, lut) for x in w.reduce_shards(cfg["S"], per, cfg["sigma"], seed=k)]
+        step, unit = (lambda: oracle.decompress_reduce(streams, per)), 2 * cfg["S"] * per
+    elif name == "activation_mix_lut":
+        x = w.activation_mix(256, 4096, seed=k)
+        step, unit = (lambda: oracle.exponent_histogram(x)), 2 * x.size
+    else:
+        x = w.gaussian(1 << 20, cfg["sigma"], seed=k) if not name.startswith("activation_mix") else \
+            w.activation_mix(256, 4096, seed=k)
+        step, unit = (lambda: oracle.decompress(oracle.compress(x, lut), x.size)), 2 * 2 * x.size
+    step()
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        step()
+        reps += 1
+    return reps * unit, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(name, budget_s=6.0):
+    """The same oracle, unchanged, run by one process per host core at once,
+    each on its own slice of the workload's distribution: the chunk-parallel
+    CPU figure.  Processes start by spawn (this runs after GPU work)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as pool:
+        res = list(pool.map(_oracle_slice_worker, [name] * cores, range(cores), [budget_s] * cores))
+    total_bytes = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    what = {"rs_local": "decompress_reduce of 8 shards x 262,144",
+            "rs_local_own": "decompress_reduce of 8 shards x 262,144",
+            "activation_mix_lut": "exponent histogram of 1,048,576"}.get(name, "compress + decompress of 1,048,576")
+    return {"value": round(total_bytes / wall / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle, one process per core", "sample": f"{what} elements per process, {budget_s:.0f} s each"}
+
+
 # ---------------------------------------------------------------------------
 def run_reference(args):
     world, rank, _, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0, None
@@ -610,9 +655,10 @@ def main():
     st = int(status.item())
     if st != 0:
         raise SystemExit(f"device status {st} ({z.status_string(st)}) during the timed region")
-    k_ms = {names[0]: statistics.mean(e[0].elapsed_time(e[1]) for e in evs)}
+    k_all = {names[0]: [e[0].elapsed_time(e[1]) for e in evs]}
     if len(names) > 1:
-        k_ms[names[1]] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        k_all[names[1]] = [e[1].elapsed_time(e[2]) for e in evs]
+    k_ms = {nm: statistics.mean(v) for nm, v in k_all.items()}
     region_ms = t_start.elapsed_time(t_end)
     kernel_ms = sum(k_ms.values())
     ms_per_step = kernel_ms if kind != "roundtrip" else region_ms / args.steps
@@ -710,9 +756,11 @@ def main():
     for nm in names:
         a = alg[nm] / (k_ms[nm] * 1e-3) / 1e9
         inp = (step_input_bytes / len(names)) / (k_ms[nm] * 1e-3) / 1e9
+        q = np.percentile(k_all[nm], [10, 50, 90])
         kernels[nm] = {"ms": round(k_ms[nm], 4), "bf16_input_gbs": round(inp, 2),
                        "algorithmic_bytes": alg[nm], "achieved_gbs": round(a, 2),
-                       "frac_of_" + peak_kind: round(a / peak, 4)}
+                       "frac_of_" + peak_kind: round(a / peak, 4),
+                       "ms_p10_median_p90": [round(float(x), 4) for x in q]}
     line = {
         "metric": "compress/decompress GB/s of BF16 input",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -734,6 +782,7 @@ def main():
         line["e2e"] = e2e
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.workload)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
