@@ -22,21 +22,24 @@
 //    from one 16-byte shared load: byte permutes give the sign-mantissa
 //    bytes, a 256-entry shared table gives each exponent's three code bits
 //    pre-spread one byte apart, accumulated into one word whose bytes are the
-//    three plane bytes.  The coded block leaves by one bulk store.  popc over
+//    three plane bytes (whole 4096-element chunks take a coder specialised
+//    for them).  The coded block leaves by one bulk store.  popc over
 //    ~(p0|p1|p2) counts the chunk's escapes; they are compacted within the
-//    chunk into a staging slot of the workspace, the count is recorded, and
-//    the chunk is added to its run's flag word (one coded chunk, plus its
-//    escapes unless a segment starts after it within its run).  When the CTA
-//    runs out of tickets, thread 0 counts the CTA's chunks (and the CTA) on
-//    the call's done counter with one release add.
-//  Phase 2: once every chunk is coded (thread 0 of each CTA polls the
-//    counter), CTA b takes run b: the escapes on the flag words of the runs
-//    back to its segment's start are its carry (the device-wide exclusive
-//    scan done O(grid) per CTA).  It
-//    scans its run's chunk counts from there, copies each chunk's staged
-//    escapes to their place in the zero-point array (clearing the staging
-//    words), and finishes the streams that end in the run (header, zero
-//    padding, size).
+//    chunk into a staging slot of the workspace, the count is recorded (plus
+//    one, so that 0 means not yet), and the chunk is added to its run's flag
+//    word (one coded chunk, plus its escapes unless a segment starts after it
+//    within its run).  When the CTA runs out of tickets, one thread counts
+//    the CTA's chunks (and the CTA) on the call's done counter with one
+//    release add.
+//  Phase 2: CTA b takes run b.  The flag words of the runs back to its
+//    segment's start (their escapes are its carry: the device-wide exclusive
+//    scan done O(grid) per CTA) and its run's chunk counts are loaded at
+//    once; both show whether they are final.  Thread 0 then polls the done
+//    counter until every chunk is coded, and what was not final is loaded
+//    again.  The CTA scans its run's chunk counts from the carry, copies each
+//    chunk's staged escapes to their place in the zero-point array (clearing
+//    the staging words; these are read only after the wait's acquire), and
+//    finishes the streams that end in the run (header, zero padding, size).
 //  The run flag words and the counter come in two sets picked by the parity
 //  of the call count of the workspace; each call clears the set the next
 //  one will use.
