@@ -63,13 +63,20 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and with runs of whitespace collapsed:
+    what the hash of a kernel's sources should follow (a comment edit does
+    not change the kernel)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_sha(names):
     h = hashlib.sha256()
-    for n in names:
-        with open(os.path.join(ROOT, "lossless_bf16_exponent_split_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
-    with open(os.path.join(ROOT, "lossless_bf16_exponent_split_gb300", "csrc", "zccl_common.cuh"), "rb") as f:
-        h.update(f.read())
+    for n in list(names) + ["zccl_common.cuh"]:
+        with open(os.path.join(ROOT, "lossless_bf16_exponent_split_gb300", "csrc", n)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
