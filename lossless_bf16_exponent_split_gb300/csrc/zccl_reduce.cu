@@ -167,6 +167,34 @@ __device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, 
     if (zbytes) bulk_g2s(sm.stage[st].zpb, t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
 }
 
+// One step's share of a thread: decode (or read) its 32 elements of the
+// stage and add them to its accumulators.  kFull: the chunk is whole, so
+// no element needs a bound check and the four groups interleave freely.
+template <bool kFull>
+__device__ __forceinline__ void fold_step(const uint8_t* blk, uint32_t L, uint32_t kind, uint32_t lut_lo,
+                                          uint32_t lut_hi, const ReduceSmem& sm, float2 (&acc)[16], bool first_step)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (kFull) L = kChunk;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
+        if (kFull || e0 < L) {
+            const uint4 o = kind == kStepStream
+                                ? decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
+                                          blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
+                                          *reinterpret_cast<const uint2*>(sm.expo + e0), sm.spread)
+                                : *reinterpret_cast<const uint4*>(blk + 2 * e0);
+            const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+                acc[4 * i + k] = first_step ? f : __fadd2_rn(acc[4 * i + k], f);
+            }
+        }
+    }
+}
+
 // All threads of the CTA: the CTA's chunks (static stride), each over its
 // steps in order.  The fp32 sums are kept as pairs and added with the
 // two-lane add (each lane rounds to nearest even exactly as a scalar add).
@@ -244,22 +272,10 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             __syncwarp();
         }
         const uint32_t lut_lo = t.lut[2 * s], lut_hi = t.lut[2 * s + 1];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-            if (e0 < L) {
-                const uint4 o = kind == kStepStream
-                                    ? decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
-                                              blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo,
-                                              lut_hi, *reinterpret_cast<const uint2*>(sm.expo + e0), sm.spread)
-                                    : *reinterpret_cast<const uint4*>(blk + 2 * e0);
-                const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-                    acc[4 * i + k] = q == 0 ? f : __fadd2_rn(acc[4 * i + k], f);
-                }
-            }
+        if (L == kChunk) {
+            fold_step<true>(blk, L, kind, lut_lo, lut_hi, sm, acc, q == 0);
+        } else {
+            fold_step<false>(blk, L, kind, lut_lo, lut_hi, sm, acc, q == 0);
         }
         if (q + 1 == Q) {
             // the chunk's offset words have had their one reader (loaded

@@ -29,7 +29,7 @@ def gpu_reduce(codec, streams, n, in_bytes=None):
 
 
 @pytest.mark.parametrize("S,n", [(1, 5000), (2, 4096), (3, 3 * 4096 + 77), (8, 100_003),
-                                 (5, 1), (4, 1023), (40, 9000)])
+                                 (5, 1), (4, 1023), (40, 9000), (2, 4 * 4096 + 3500)])
 def test_reduce_matches_oracle(codec, S, n):
     shards = [workloads.special_values(n, seed=10 * S + s, frac=0.05) for s in range(S)]
     luts = [oracle.lut_from_sigma(1.0), oracle.lut_from_sigma(0.5), bytes([0, 255, 1, 2, 3, 254, 127])]
