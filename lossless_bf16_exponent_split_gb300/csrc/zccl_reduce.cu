@@ -33,6 +33,9 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kStages = 3;
+// Shared memory (three stages, about 35 KB) admits 6 CTAs per SM; registers
+// are capped to match, so neither instance falls below it.
+constexpr int kCtasPerSm = 6;
 
 // One stage of the ring: a shard's block and its zero-point run, or a chunk
 // of plain BF16 (the rank's own shard, or the output being accumulated into).
@@ -110,13 +113,11 @@ struct StepOffsets {
 };
 
 template <bool kPlain>
-__device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t j, uint32_t total)
+__device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t c, uint32_t q, uint32_t total)
 {
     StepOffsets o{0, 0, 0};
-    const uint32_t Q = steps_per_chunk<kPlain>(a);
-    const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
     uint32_t s = 0;
-    if (c >= total || step_kind<kPlain>(a, j % Q, &s) != kStepStream) return o;
+    if (c >= total || step_kind<kPlain>(a, q, &s) != kStepStream) return o;
     const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
     const uint64_t idx = (uint64_t)s * total + c;
     o.base = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks);
@@ -125,18 +126,14 @@ __device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_
     return o;
 }
 
-// Thread 0: queue step j of this CTA (chunk blockIdx.x + (j / Q) * gridDim.x,
-// step j % Q) into stage j % kStages.
+// Thread 0: queue step q of chunk c into stage st.
 template <bool kPlain>
-__device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t j,
-                                           uint32_t total, const StepOffsets& off)
+__device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t c,
+                                           uint32_t q, int st, uint32_t total, const StepOffsets& off)
 {
-    const uint32_t Q = steps_per_chunk<kPlain>(a);
-    const uint32_t c = blockIdx.x + (j / Q) * gridDim.x;
     if (c >= total) return;
     uint32_t s = 0;
-    const uint32_t kind = step_kind<kPlain>(a, j % Q, &s);
-    const int st = j % kStages;
+    const uint32_t kind = step_kind<kPlain>(a, q, &s);
     const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
     if (kind != kStepStream) {  // plain BF16: whole 16-byte pieces by bulk copy, the rest by plain loads
         const uint16_t* src = (kind == kStepLocal ? a.local : a.out) + (uint64_t)c * kChunk;
@@ -204,11 +201,25 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t total = (uint32_t)units_of(a.n);
     const uint32_t Q = steps_per_chunk<kPlain>(a);
-    StepOffsets ahead{0, 0, 0};  // thread 0: offsets of the next step to queue
+    // thread 0: `ahead` holds the offsets of the next step to queue, at
+    // (ic, iq); (pc, pq) is the step after it
+    StepOffsets ahead{0, 0, 0};
+    uint32_t pc = blockIdx.x, pq = 0, ic = 0, iq = 0;
+    auto advance = [&]() {
+        if (++pq == Q) {
+            pq = 0;
+            pc += gridDim.x;
+        }
+    };
     if (tid == 0) {
-        for (uint32_t j = 0; j + 1 < kStages; ++j)
-            issue_step<kPlain>(a, sm, t, j, total, load_offsets<kPlain>(a, j, total));
-        ahead = load_offsets<kPlain>(a, kStages - 1, total);
+        for (int j = 0; j + 1 < kStages; ++j) {
+            issue_step<kPlain>(a, sm, t, pc, pq, j, total, load_offsets<kPlain>(a, pc, pq, total));
+            advance();
+        }
+        ic = pc;
+        iq = pq;
+        ahead = load_offsets<kPlain>(a, pc, pq, total);
+        advance();
     }
 
     float2 acc[16];
@@ -242,8 +253,11 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         // with step j + kStages - 1 (this barrier is also the previous
         // step's end)
         if (tid == 0) {
-            issue_step<kPlain>(a, sm, t, j + kStages - 1, total, ahead);
-            ahead = load_offsets<kPlain>(a, j + kStages, total);
+            issue_step<kPlain>(a, sm, t, ic, iq, (j + kStages - 1) % kStages, total, ahead);
+            ic = pc;
+            iq = pq;
+            ahead = load_offsets<kPlain>(a, pc, pq, total);
+            advance();
         }
         if (kind == kStepStream) {
             uint32_t esc = 0;
@@ -317,7 +331,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
 }
 
 template <bool kPlain>
-__global__ void __launch_bounds__(kThreads) reduce_kernel(const ReduceArgs a)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const ReduceArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     ReduceSmem& sm = *reinterpret_cast<ReduceSmem*>(smem_raw);
