@@ -51,7 +51,7 @@ struct __align__(16) ReduceSmem {
     uint64_t bar[kStages];
     uint32_t zdelta[kStages];
     uint32_t zcount[kStages];
-    uint32_t scan[kThreads / 32];
+    uint32_t scan[2][kThreads / 32];  // the warps' escape totals, by step parity
     uint32_t abort;
     uint32_t last;
     uint32_t spread[256];  // spread_nibbles of every byte
@@ -237,21 +237,39 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         const uint32_t L = slots_of(valid);
         if (!mbar_wait(&sm.bar[st], (j / kStages) & 1)) atomicExch(&sm.abort, 1u);
         uint8_t* blk = sm.stage[st].blk;
+        uint32_t esc = 0, incl = 0;
         if (kind != kStepStream) {  // plain BF16: the last < 8 values by plain loads
             const uint32_t done = valid & ~7u;
             if (tid < (int)(valid - done)) {
                 const uint16_t* src = kind == kStepLocal ? a.local : a.out;
                 reinterpret_cast<uint16_t*>(blk)[done + tid] = src[first + done + tid];
             }
+        } else {
+            if (tid < (int)(L / 32)) {
+                const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+                const uint32_t w0 = 32u * tid;
+                const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
+                                       : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+                esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
+            }
+            incl = __popc(esc);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sm.scan[j & 1][warp] = incl;
         }
+        // the step's one barrier: stage st has landed for every thread, the
+        // warps' escape totals are posted, and every thread is past step
+        // j - 1, so its stage is free (a warp reaches the next step's
+        // totals, in the other parity's slots, only through this barrier)
         __syncthreads();
         if (sm.abort) {
             if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
             break;
         }
-        // every thread is past step j - 1, so its stage is free: refill it
-        // with step j + kStages - 1 (this barrier is also the previous
-        // step's end)
+        // refill the freed stage with step j + kStages - 1
         if (tid == 0) {
             issue_step<kPlain>(a, sm, t, ic, iq, (j + kStages - 1) % kStages, total, ahead);
             ic = pc;
@@ -260,18 +278,15 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
             advance();
         }
         if (kind == kStepStream) {
-            uint32_t esc = 0;
-            if (tid < (int)(L / 32)) {
-                const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-                const uint32_t w0 = 32u * tid;
-                const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
-                                       : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-                esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
+            uint32_t before = 0, agg = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const uint32_t v = sm.scan[j & 1][w];
+                before += w < warp ? v : 0u;
+                agg += v;
             }
-            uint32_t agg;
-            const uint32_t excl = block_exclusive_scan<kThreads, uint32_t, false>((uint32_t)__popc(esc), sm.scan, &agg);
             if (agg == sm.zcount[st]) {
-                const uint8_t* src = sm.stage[st].zpb + sm.zdelta[st] + excl;
+                const uint8_t* src = sm.stage[st].zpb + sm.zdelta[st] + before + incl - __popc(esc);
                 uint32_t m = esc, jj = 0;
                 while (m) {
                     const uint32_t b = __ffs(m) - 1;
