@@ -7,7 +7,9 @@ the codec's hot path over one batch: compress a batch, and decompress the
 stream compressed one step earlier (so the stream read by decompress is not
 L2-resident, as it would not be after crossing the network).  Three rotating
 buffer sets, 316 MB touched per step (> 129 MB L2), keep every step's inputs
-out of L2.  Other workloads (--workload): activation_mix (compress +
+out of L2.  Within the timed region each op's K launches run back to back
+between one pair of CUDA events; the same launches timed one at a time,
+each between its own events, are reported beside them.  Other workloads (--workload): activation_mix (compress +
 decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
 rs_local (decompress-reduce of 8 shards), rs_local_own (the same with the rank's own shard
 uncompressed), activation_mix_lut (the exponent histogram pass that measures
@@ -510,18 +512,15 @@ def main():
         alg = {"compress": 2 * n + stream_bytes, "decompress": stream_bytes + 2 * n}
         step_input_bytes = 2 * 2 * n
 
-        def step(k, ev=None):
-            r = k % R
-            if ev:
-                ev[0].record(stream)
-            comp(r)
-            if ev:
-                ev[1].record(stream)
-            decomp((k - 1) % R)
-            if ev:
-                ev[2].record(stream)
+        # decompress reads a stream compressed one launch before or after in
+        # the rotation, never the one just written (part of it is still in L2):
+        # not in the interleaved single-launch timing, nor at the start of the
+        # decompress batch, which follows the whole compress batch
+        off = -1 if (args.warmup + args.steps) % R != args.warmup % R else 1
+        ops = [("compress", lambda k: comp(k % R)), ("decompress", lambda k: decomp((k + off) % R))]
         cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
-                     "step": "compress batch k + decompress stream of batch k-1",
+                     "step": "compress batch k + decompress the stream of batch k-1 (k+1 in the rotation "
+                             "when k-1's buffer is the one the compress batch wrote last)",
                      "l2": "3 rotating buffer sets, >316 MB touched per step (> 129 MB L2)"}
     elif kind == "batched":
         m = extra
@@ -552,13 +551,7 @@ def main():
         alg = {"compress": 2 * total_n + sb}
         step_input_bytes = 2 * total_n
 
-        def step(k, ev=None):
-            if ev:
-                ev[0].record(stream)
-            comp()
-            if ev:
-                ev[1].record(stream)
-                ev[2].record(stream)
+        ops = [("compress", lambda k: comp())]
         cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
                      "step": "one batched compress of all static+dynamic segments",
                      "l2": "input 537 MB > 129 MB L2"}
@@ -574,13 +567,7 @@ def main():
         alg = {"histogram": 2 * n + 256 * 8}
         step_input_bytes = 2 * n
 
-        def step(k, ev=None):
-            if ev:
-                ev[0].record(stream)
-            hist_call(k % R)
-            if ev:
-                ev[1].record(stream)
-                ev[2].record(stream)
+        ops = [("histogram", lambda k: hist_call(k % R))]
         hist_call(0)
         hh0 = hist.cpu().numpy().view(np.uint64).astype(np.float64)
         lut_data = z.zccl_lut_from_histogram(hist.cpu().numpy().view(np.uint64))
@@ -596,26 +583,32 @@ def main():
         S = len(shards)
         n = shards[0].size
         codec = z.Codec(dev)
-        streams, sizes = [], []
-        for s_, x in enumerate(shards):
-            if s_ == local_pos:
-                streams.append(None)
-                sizes.append(None)
-                continue
-            o, nbt = codec.compress(tdev(x), lut)
-            streams.append(o)
-            sizes.append(nbt)
-        torch.cuda.synchronize()
-        sizes_h = [0 if v is None else int(v.item()) for v in sizes]
-        ptrs = torch.tensor([0 if o is None else o.data_ptr() for o in streams], dtype=torch.int64, device=dev)
-        inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
-        local = tdev(shards[local_pos]) if local_pos is not None else None
-        y = torch.empty(n, dtype=torch.int16, device=dev)
+        # three copies of the step's inputs (streams, local shard) and outputs,
+        # used in rotation: two other calls (442 MB) run between two reads of one
+        R = 3
+        sets = []
+        for _ in range(R):
+            streams, sizes = [], []
+            for s_, x in enumerate(shards):
+                if s_ == local_pos:
+                    streams.append(None)
+                    sizes.append(None)
+                    continue
+                o, nbt = codec.compress(tdev(x), lut)
+                streams.append(o)
+                sizes.append(nbt)
+            torch.cuda.synchronize()
+            sizes_h = [0 if v is None else int(v.item()) for v in sizes]
+            ptrs = torch.tensor([0 if o is None else o.data_ptr() for o in streams], dtype=torch.int64, device=dev)
+            inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
+            local = tdev(shards[local_pos]) if local_pos is not None else None
+            y = torch.empty(n, dtype=torch.int16, device=dev)
+            sets.append((streams, ptrs, inb, local, y))
         wsb = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, n, S)
         ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-        def red():
+        def red(k):
+            _, ptrs, inb, local, y = sets[k % R]
             if local is None:
                 z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n,
                                                  ws.data_ptr(), wsb, st_ptr, h), "decompress_reduce")
@@ -624,28 +617,23 @@ def main():
                                                        local_pos, 0, y.data_ptr(), n, ws.data_ptr(), wsb, st_ptr,
                                                        h), "decompress_reduce_local")
         names = ["decompress_reduce"]
-        alg = {"decompress_reduce": sum(sizes_h) + (2 * n if local is not None else 0) + 2 * n}
+        alg = {"decompress_reduce": sum(sizes_h) + (2 * n if local_pos is not None else 0) + 2 * n}
         step_input_bytes = 2 * S * n
-
-        def step(k, ev=None):
-            flush.zero_()  # L2 flush (512 MB write), outside the kernel events
-            if ev:
-                ev[0].record(stream)
-            red()
-            if ev:
-                ev[1].record(stream)
-                ev[2].record(stream)
+        ops = [("decompress_reduce", red)]
         cfg_extra = {"n": n, "shards": S, "stream_bytes_total": sum(sizes_h),
                      "step": "one fused decompress+reduce of S shards"
-                             + (f" (shard {local_pos} uncompressed)" if local is not None else ""),
-                     "l2": "512 MB write between steps flushes L2 (outside kernel events)"}
+                             + (f" (shard {local_pos} uncompressed)" if local_pos is not None else ""),
+                     "l2": f"{R} rotating copies of the inputs and output; "
+                           f"{(R - 1) * (sum(sizes_h) + 2 * n + (2 * n if local_pos is not None else 0)) >> 20} MiB "
+                           "touched between two reads of one (> 129 MB L2)"}
 
     # ---- warm-up, then K timed steps ----
     for k in range(args.warmup):
-        step(k + 1)
+        for _, fn in ops:
+            fn(k + 1)
     torch.cuda.synchronize()
     status.zero_()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    op_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(pg, dev)
@@ -653,12 +641,19 @@ def main():
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         # a ~1 ms GPU sleep before the start event gives the host a head start,
-        # so no step's events bracket time the GPU spends waiting for the host
-        # to enqueue (the sleep itself is outside the timed region)
+        # so no event brackets time the GPU spends waiting for the host to
+        # enqueue (the sleep itself is outside the timed region)
         torch.cuda._sleep(2_000_000)
         t_start.record(stream)
-        for k in range(args.steps):
-            step(args.warmup + 1 + k, evs[k])
+        # the K steps' work op by op: each op's K launches run back to back
+        # between one pair of events, so a launch's time is its share of that
+        # span (an event pair around every launch would also time the event's
+        # wait for the previous kernel to drain)
+        for (nm, fn), (e0, e1) in zip(ops, op_ev):
+            e0.record(stream)
+            for k in range(args.steps):
+                fn(args.warmup + 1 + k)
+            e1.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -666,15 +661,26 @@ def main():
     st = int(status.item())
     if st != 0:
         raise SystemExit(f"device status {st} ({z.status_string(st)}) during the timed region")
-    k_all = {names[0]: [e[0].elapsed_time(e[1]) for e in evs]}
-    if len(names) > 1:
-        k_all[names[1]] = [e[1].elapsed_time(e[2]) for e in evs]
-    k_ms = {nm: statistics.mean(v) for nm, v in k_all.items()}
+    k_ms = {nm: e0.elapsed_time(e1) / args.steps for (nm, _), (e0, e1) in zip(ops, op_ev)}
     region_ms = t_start.elapsed_time(t_end)
-    kernel_ms = sum(k_ms.values())
-    ms_per_step = kernel_ms if kind != "roundtrip" else region_ms / args.steps
-    ms_per_step = max_over_ranks(pg, ms_per_step, dev)
+    ms_per_step = max_over_ranks(pg, region_ms / args.steps, dev)
     value = aggregate_gbs(world, step_input_bytes, ms_per_step)
+
+    # ---- the same launches one at a time, each between its own events ----
+    # (outside the timed region: what a caller timing a single call sees)
+    S1 = min(args.steps, 10)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(S1)]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)
+    for k in range(S1):
+        sev[k][0].record(stream)
+        for i, (_, fn) in enumerate(ops):
+            fn(args.warmup + args.steps + 1 + k)
+            sev[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} after the single-launch timing")
+    single = {nm: [sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(S1)] for i, (nm, _) in enumerate(ops)}
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
@@ -767,11 +773,15 @@ def main():
     for nm in names:
         a = alg[nm] / (k_ms[nm] * 1e-3) / 1e9
         inp = (step_input_bytes / len(names)) / (k_ms[nm] * 1e-3) / 1e9
-        q = np.percentile(k_all[nm], [10, 50, 90])
-        kernels[nm] = {"ms": round(k_ms[nm], 4), "bf16_input_gbs": round(inp, 2),
-                       "algorithmic_bytes": alg[nm], "achieved_gbs": round(a, 2),
+        q = np.percentile(single[nm], [10, 50, 90])
+        a1 = alg[nm] / (float(q[1]) * 1e-3) / 1e9
+        kernels[nm] = {"ms": round(k_ms[nm], 4), "timing": f"{args.steps} launches back to back, one event pair",
+                       "bf16_input_gbs": round(inp, 2), "algorithmic_bytes": alg[nm], "achieved_gbs": round(a, 2),
                        "frac_of_" + peak_kind: round(a / peak, 4),
-                       "ms_p10_median_p90": [round(float(x), 4) for x in q]}
+                       "single_launch_evented": {"launches": len(single[nm]),
+                                                 "ms_p10_median_p90": [round(float(x), 4) for x in q],
+                                                 "achieved_gbs_median": round(a1, 2),
+                                                 "frac_of_" + peak_kind: round(a1 / peak, 4)}}
     line = {
         "metric": "compress/decompress GB/s of BF16 input",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -780,6 +790,8 @@ def main():
         "config": {"workload": args.workload, "desc": workload_desc(args.workload), **cfg_extra,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": dom, "launches": OP_KERNELS[dom],
+                     "duration": f"mean of {args.steps} back-to-back launches in the timed region, "
+                                 "one CUDA event pair on the launching stream",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(dom, args.workload),
