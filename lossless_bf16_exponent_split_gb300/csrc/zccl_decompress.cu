@@ -17,7 +17,9 @@
 //    atomic arrival counter) runs one segmented exclusive scan over the range
 //    totals -- the inverse of the encoder's device-wide scan -- and checks
 //    each stream's total against its header.  It serves S streams at once
-//    for the fused reduction.
+//    for the fused reduction.  It is launched as a programmatic dependent of
+//    the preceding work and waits for it first, so its launch overlaps that
+//    work's tail.
 //  decompress_kernel  one cooperative kernel with no grid barrier: each CTA
 //    counts the escapes of its own run of chunks from their planes and
 //    publishes the run total as a flag word, sums the earlier runs' totals
@@ -110,6 +112,9 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
     __shared__ ScanSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t units = (uint32_t)units_of(a.n);
+    // launched as a programmatic dependent of whatever precedes it in the
+    // stream: nothing is read before that work is complete and visible
+    pdl_wait();
     const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;  // ranges per stream
     const uint32_t nr = rps * a.S;
 
@@ -589,8 +594,7 @@ int occupancy(K kernel, size_t smem)
 
 cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream)
 {
-    escape_scan_kernel<<<grid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(escape_scan_kernel, grid, kThreads, 0, stream, a);
 }
 
 cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream)

@@ -22,7 +22,10 @@
 //
 // Overwrite mode zeroes the histogram in a one-CTA kernel that the counting
 // kernel follows by programmatic dependent launch: counting starts at once
-// and only the final global adds wait for the zeroing.
+// and only the final global adds wait for the zeroing.  The first kernel is
+// itself launched as a programmatic dependent of the preceding work in the
+// stream and waits for it before anything else, so its launch overlaps that
+// work's tail.
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -62,13 +65,19 @@ __device__ __forceinline__ void count_high(uint32_t column, uint32_t bits)
 
 __global__ void __launch_bounds__(256) hist_zero_kernel(uint64_t* hist)
 {
+    // the preceding work (which may write the input or the histogram) first
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     hist[threadIdx.x] = 0;
 }
 
 __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
-    hist_kernel(const uint16_t* in, uint64_t n, unsigned long long* hist)
+    hist_kernel(const uint16_t* in, uint64_t n, unsigned long long* hist, bool wait_first)
 {
+    // accumulate mode: launched right behind the preceding work, which may
+    // write the input; overwrite mode: behind the zeroing kernel, which
+    // starts it only once that work is complete
+    if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ uint32_t cnt[];  // [256][32]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < 256 * 32; i += kHistThreads) cnt[i] = 0;
@@ -147,16 +156,21 @@ cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint64_t* hist, boo
     cfg.dynamicSmemBytes = kHistSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     if (!accumulate) {
-        hist_zero_kernel<<<1, 256, 0, stream>>>(hist);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t zc = {};
+        zc.gridDim = dim3(1);
+        zc.blockDim = dim3(256);
+        zc.stream = stream;
+        zc.attrs = attr;
+        zc.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&zc, hist_zero_kernel, hist);
         if (e != cudaSuccess) return e;
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, hist_kernel, in, n, reinterpret_cast<unsigned long long*>(hist));
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, hist_kernel, in, n, reinterpret_cast<unsigned long long*>(hist), accumulate);
 }
 
 }  // namespace zccl
