@@ -336,7 +336,7 @@ __device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& s
         }
     }
     // steps still in flight after an early stop at step j: j + 1 .. j + kStages - 2
-    // (step j + kStages - 1 is issued only after step j's first barrier); wait for
+    // (step j + kStages - 1 is issued only after step j's barrier); wait for
     // them (bounded)
     if (tid == 0 && sm.abort) {
         for (uint32_t jj = j + 1; jj + 1 < j + kStages; ++jj) {
