@@ -8,8 +8,10 @@ stream compressed one step earlier (so the stream read by decompress is not
 L2-resident, as it would not be after crossing the network).  Three rotating
 buffer sets, 316 MB touched per step (> 129 MB L2), keep every step's inputs
 out of L2.  Within the timed region each op's K launches run back to back
-between one pair of CUDA events; the same launches timed one at a time,
-each between its own events, are reported beside them.  Other workloads (--workload): activation_mix (compress +
+between one pair of CUDA events.  After it, the same launches are timed one
+at a time (each between its own events), and once more back to back with
+events at six group boundaries for a spread; both are reported beside the
+timed means.  Other workloads (--workload): activation_mix (compress +
 decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
 rs_local (decompress-reduce of 8 shards), rs_local_own (the same with the rank's own shard
 uncompressed), activation_mix_lut (the exponent histogram pass that measures
@@ -682,6 +684,26 @@ def main():
         raise SystemExit(f"device status {int(status.item())} after the single-launch timing")
     single = {nm: [sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(S1)] for i, (nm, _) in enumerate(ops)}
 
+    # ---- spread: the same back-to-back runs again, with events at the
+    # boundaries of up to 6 groups (each inner event adds a drain, so these
+    # group means are a little above the timed region's) ----
+    n_groups = min(args.steps, 6)
+    bounds = [round(i * args.steps / n_groups) for i in range(n_groups + 1)]
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in bounds] for _ in ops]
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)
+    for (nm, fn), evs in zip(ops, gev):
+        evs[0].record(stream)
+        for g in range(n_groups):
+            for k in range(bounds[g], bounds[g + 1]):
+                fn(args.warmup + args.steps + S1 + 1 + k)
+            evs[g + 1].record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} after the spread pass")
+    k_groups = {nm: [evs[g].elapsed_time(evs[g + 1]) / (bounds[g + 1] - bounds[g]) for g in range(n_groups)]
+                for (nm, _), evs in zip(ops, gev)}
+
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
     if kind == "roundtrip" and not args.no_e2e:
@@ -775,7 +797,10 @@ def main():
         inp = (step_input_bytes / len(names)) / (k_ms[nm] * 1e-3) / 1e9
         q = np.percentile(single[nm], [10, 50, 90])
         a1 = alg[nm] / (float(q[1]) * 1e-3) / 1e9
-        kernels[nm] = {"ms": round(k_ms[nm], 4), "timing": f"{args.steps} launches back to back, one event pair",
+        qg = np.percentile(k_groups[nm], [10, 50, 90])
+        kernels[nm] = {"ms": round(k_ms[nm], 4),
+                       "timing": f"{args.steps} launches back to back, one event pair",
+                       "spread_pass_group_ms_p10_median_p90": [round(float(x), 4) for x in qg],
                        "bf16_input_gbs": round(inp, 2), "algorithmic_bytes": alg[nm], "achieved_gbs": round(a, 2),
                        "frac_of_" + peak_kind: round(a / peak, 4),
                        "single_launch_evented": {"launches": len(single[nm]),
@@ -790,8 +815,8 @@ def main():
         "config": {"workload": args.workload, "desc": workload_desc(args.workload), **cfg_extra,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": dom, "launches": OP_KERNELS[dom],
-                     "duration": f"mean of {args.steps} back-to-back launches in the timed region, "
-                                 "one CUDA event pair on the launching stream",
+                     "duration": f"mean of {args.steps} back-to-back launches in the timed region "
+                                 "(CUDA events on the launching stream)",
                      "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(dom, args.workload),
