@@ -26,13 +26,16 @@ struct DeviceInfo {
     std::once_flag once;
     int sms = 0;
     int compress_per_sm = 1;
-    int compress_per_sm_batched = 1;
+    // the batched kernel's shared memory grows with the segment count: its
+    // occupancy for 2^b segments, b = 0 .. log2(ZCCL_MAX_SEGMENTS)
+    int compress_per_sm_batched[13] = {};
     int scan_per_sm = 1;
     int decompress_per_sm = 1;
     int reduce_per_sm_small = 1;  // S <= kSmallShards
     int reduce_per_sm_large = 1;  // any S <= ZCCL_MAX_SHARDS
 };
 constexpr uint32_t kSmallShards = 32;
+static_assert(ZCCL_MAX_SEGMENTS == 1u << 12, "one occupancy bucket per power of two up to the segment limit");
 DeviceInfo g_dev[kMaxDevices];
 
 // SM count and kernel occupancy of the current device, computed once.
@@ -46,7 +49,7 @@ const DeviceInfo* device_info()
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         d.sms = sms > 0 ? sms : 1;
         d.compress_per_sm = compress_ctas_per_sm(1);
-        d.compress_per_sm_batched = compress_ctas_per_sm(ZCCL_MAX_SEGMENTS);
+        for (int b = 0; b < 13; ++b) d.compress_per_sm_batched[b] = compress_ctas_per_sm(1u << b);
         d.scan_per_sm = scan_ctas_per_sm();
         d.decompress_per_sm = decompress_ctas_per_sm();
         d.reduce_per_sm_small = reduce_ctas_per_sm(kSmallShards);
@@ -265,7 +268,11 @@ zccl_status_t zccl_compress_batched(const zccl_segment_t* d_segs, uint32_t n_seg
     a.counts = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.counts);
     a.stage = (uint8_t*)d_ws + l.stage;
     a.status = d_status;
-    return launch_compress(a, grid_for(max_units, dev->compress_per_sm_batched, dev->sms), stream) == cudaSuccess
+    // occupancy of the next power of two at or above n_segs: that needs at
+    // least this call's shared memory, so the grid stays co-resident
+    int b = 0;
+    while ((1u << b) < n_segs) ++b;
+    return launch_compress(a, grid_for(max_units, dev->compress_per_sm_batched[b], dev->sms), stream) == cudaSuccess
                ? ZCCL_OK
                : ZCCL_ERR_CUDA;
 }
