@@ -287,6 +287,24 @@ def workload_desc(name):
     return workloads.CONFIGS[name]["desc"]
 
 
+def decompress_offset(warmup: int, steps: int, R: int) -> int:
+    """Rotation offset of the stream the round trip's decompress reads at
+    step k: buffer (k + offset) mod R, with compress writing buffer k mod R.
+    -1 (the previous step's stream) unless the timed decompress batch would
+    then start on the buffer the timed compress batch wrote last, still partly
+    in L2; then +1.  Never 0, which would read the stream just written in the
+    interleaved single-launch timing."""
+    last = (warmup + steps) % R
+    return -1 if warmup % R != last else 1
+
+
+def group_bounds(steps: int, groups: int = 6) -> list:
+    """Launch indices bounding up to `groups` non-empty, near-equal groups of
+    `steps` back-to-back launches (for the spread pass)."""
+    g = min(steps, groups)
+    return [round(i * steps / g) for i in range(g + 1)]
+
+
 def make_inputs(name, seed):
     """Host arrays for a workload: (kind, payload(s), sigma, extra)."""
     from lossless_bf16_exponent_split_gb300 import workloads as w
@@ -518,7 +536,7 @@ def main():
         # the rotation, never the one just written (part of it is still in L2):
         # not in the interleaved single-launch timing, nor at the start of the
         # decompress batch, which follows the whole compress batch
-        off = -1 if (args.warmup + args.steps) % R != args.warmup % R else 1
+        off = decompress_offset(args.warmup, args.steps, R)
         ops = [("compress", lambda k: comp(k % R)), ("decompress", lambda k: decomp((k + off) % R))]
         cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
                      "step": "compress batch k + decompress the stream of batch k-1 (k+1 in the rotation "
@@ -687,8 +705,8 @@ def main():
     # ---- spread: the same back-to-back runs again, with events at the
     # boundaries of up to 6 groups (each inner event adds a drain, so these
     # group means are a little above the timed region's) ----
-    n_groups = min(args.steps, 6)
-    bounds = [round(i * args.steps / n_groups) for i in range(n_groups + 1)]
+    bounds = group_bounds(args.steps)
+    n_groups = len(bounds) - 1
     gev = [[torch.cuda.Event(enable_timing=True) for _ in bounds] for _ in ops]
     torch.cuda.synchronize()
     torch.cuda._sleep(2_000_000)
