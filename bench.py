@@ -32,6 +32,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -189,7 +190,12 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw nvidia-smi record goes where ZCCL_BENCH_CLOCKS_DIR says (kept
+        # for inspection), else to a temporary file removed after the summary
+        keep = os.environ.get("ZCCL_BENCH_CLOCKS_DIR")
+        base = keep if keep else tempfile.gettempdir()
+        self.keep = bool(keep)
+        self.path = os.path.join(base, f"zccl_clocks_{os.getpid()}.csv")
         self.poller = None
 
     def __enter__(self):
@@ -218,6 +224,16 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        try:
+            return self._summary()
+        finally:
+            if not self.keep:
+                try:
+                    os.remove(self.path)
+                except OSError:
+                    pass
+
+    def _summary(self):
         p = self.poller
         if p is not None and p.samples:
             return {"sm_mhz": statistics.median(p.samples), "sm_max_mhz": p.max_mhz, "samples": len(p.samples),
