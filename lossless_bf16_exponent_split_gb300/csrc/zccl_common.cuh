@@ -97,6 +97,20 @@ constexpr uint64_t kValid = 1ull << 63;
 // scans at the end of a pass.
 constexpr uint32_t kRangeChunks = 32;
 
+// A chunk's quarter word, written by the escape scan for the fused
+// reduction: the escapes before quarter q (q = 1, 2, 3; a quarter is 1024
+// slots) in bits 16(q-1) .. 16q-1, and the chunk's total in bits 48..63.
+// Quarter q's escapes are those from quarter_before(q) up to quarter_end(q).
+__host__ __device__ inline uint32_t quarter_before(uint64_t qi, uint32_t q)
+{
+    return q == 0 ? 0u : (uint32_t)(qi >> (16 * (q - 1))) & 0xFFFFu;
+}
+__host__ __device__ inline uint32_t quarter_end(uint64_t qi, uint32_t q)
+{
+    return (uint32_t)(qi >> (16 * q)) & 0xFFFFu;
+}
+__host__ __device__ inline uint32_t chunk_escapes(uint64_t qi) { return (uint32_t)(qi >> 48); }
+
 // A bounded wait gives up after this long (then reports ZCCL_ERR_TIMEOUT).
 constexpr uint64_t kSpinTimeoutNs = 1000000000ull;
 
@@ -266,6 +280,68 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory accesses by 32-bit shared address.  They are volatile so
+// that they stay where they are written relative to the waits (also
+// volatile) that make their data valid.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_u128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_u8(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v));
+}
+__device__ __forceinline__ void sts_u32(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v));
+}
+__device__ __forceinline__ uint64_t lds_u64w(uint32_t a)
+{
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_u64(uint32_t a, uint64_t v)
+{
+    asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v));
+}
+
+// 16-byte asynchronous copy global -> shared by one thread (cp.async, L2
+// only): src_bytes of 16 are read, the rest of the 16 bytes zero-filled.
+// Both addresses 16-byte aligned.  Completion: cp_async_commit() closes the
+// thread's current group; cp_async_wait<N>() waits until at most N of its
+// groups are pending.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes = 16)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- warp / block helpers ---------------------------------------------------

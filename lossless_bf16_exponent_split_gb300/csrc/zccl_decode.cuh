@@ -1,6 +1,7 @@
 // zccl_decode.cuh -- rebuilding BF16 values from a chunk block: code planes
-// -> LUT exponents (or escaped exponents) + sign-mantissa bytes.  Shared by
-// the decompress and the fused decompress-reduce kernels.
+// -> LUT exponents (or escaped exponents) + sign-mantissa bytes.  Used by
+// the decompress kernel; the fused decompress-reduce kernel shares the
+// nibble spreading and the partial store.
 //
 // Page: "ZipCCL: Efficient Lossless Data Compression of Communication
 // Collectives for Accelerating LLM Training", technical summary 2.B
@@ -54,15 +55,6 @@ __device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, 
     return decode8_nibbles(N, smb, lut_lo, lut_hi, xe);
 }
 
-// The same with the bit spreading looked up: spread[b] = spread_nibbles(b),
-// a 256-word table in shared memory (three loads instead of ~18 ALU ops).
-__device__ __forceinline__ uint4 decode8(uint2 smb, uint32_t pb0, uint32_t pb1, uint32_t pb2, uint32_t lut_lo,
-                                         uint32_t lut_hi, uint2 xe, const uint32_t* spread)
-{
-    const uint32_t N = spread[pb0] | (spread[pb1] << 1) | (spread[pb2] << 2);
-    return decode8_nibbles(N, smb, lut_lo, lut_hi, xe);
-}
-
 __device__ __forceinline__ void store_partial(uint16_t* dst, uint4 o, uint32_t count)
 {
 #pragma unroll
@@ -72,14 +64,6 @@ __device__ __forceinline__ void store_partial(uint16_t* dst, uint4 o, uint32_t c
             dst[q] = (uint16_t)(w >> (16 * (q & 1)));
         }
     }
-}
-
-// fp32 -> BF16, round to nearest, ties to even; any NaN -> 0x7FC0.
-__device__ __forceinline__ uint32_t rne_bf16(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
-    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
 }
 
 }  // namespace zccl

@@ -12,8 +12,9 @@
 //  escape_scan_kernel (used by the fused reduction, zccl_reduce.cu)  reads only the code planes (3/8 byte per element).
 //    One CTA per range of 32 chunks: each warp counts the escapes of 8 chunks
 //    with 16-byte loads (all issued first) and popc of ~(p0|p1|p2), and the
-//    CTA records each chunk's count and prefix within the range plus the
-//    range total.  No CTA waits for another: the CTA that finishes last (an
+//    CTA records each chunk's count, the escapes before each of its quarters
+//    (1024 slots: the share of one reducing warp) and its prefix within the
+//    range, plus the range total.  No CTA waits for another: the CTA that finishes last (an
 //    atomic arrival counter) runs one segmented exclusive scan over the range
 //    totals -- the inverse of the encoder's device-wide scan -- and checks
 //    each stream's total against its header.  It serves S streams at once
@@ -50,9 +51,9 @@ constexpr int kThreads = 128;
 // ============================================================================
 struct __align__(16) ScanSmem {
     uint64_t scan64[kThreads / 32];
+    uint64_t qinfo[kRangeChunks];
     uint32_t scan[kThreads / 32];
     uint32_t scan_f[kThreads / 32];
-    uint32_t cnt[kRangeChunks];
     uint32_t hdr_ok;
     uint32_t last;
 };
@@ -107,7 +108,42 @@ __device__ __forceinline__ uint32_t warp_chunk_escapes(const uint8_t* blk, uint3
     return c;
 }
 
-__global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
+// Escapes of one chunk, by one warp: lane l counts slots [128 l, 128 l + 128)
+// (16 bytes of each plane), so lanes 8q .. 8q + 7 cover quarter q.  Returns
+// the chunk's quarter word: escapes before quarters 1, 2, 3 and the chunk
+// total, 16 bits each (quarter_before / quarter_end).  p holds the lane's plane words
+// for a whole chunk (valid == 4096); otherwise they are loaded here, masked
+// to the valid slots.
+__device__ __forceinline__ uint64_t warp_chunk_quarters(const uint4 (&p)[3], const uint8_t* blk, uint32_t valid)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t e = 0;
+    if (valid == kChunk) {
+        e = __popc(~(p[0].x | p[1].x | p[2].x)) + __popc(~(p[0].y | p[1].y | p[2].y)) +
+            __popc(~(p[0].z | p[1].z | p[2].z)) + __popc(~(p[0].w | p[1].w | p[2].w));
+    } else {
+        const uint32_t L = slots_of(valid);
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k) {
+            const uint32_t w = 4u * lane + k;
+            if (w < L / 32) {
+                const uint32_t w0 = 32u * w;
+                const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
+                                       : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
+                e += __popc(~(pw[w] | pw[L / 32 + w] | pw[L / 16 + w]) & vmask);
+            }
+        }
+    }
+    e += __shfl_xor_sync(0xffffffffu, e, 1);
+    e += __shfl_xor_sync(0xffffffffu, e, 2);
+    e += __shfl_xor_sync(0xffffffffu, e, 4);
+    const uint64_t q0 = __shfl_sync(0xffffffffu, e, 0), q1 = __shfl_sync(0xffffffffu, e, 8);
+    const uint64_t q2 = __shfl_sync(0xffffffffu, e, 16), q3 = __shfl_sync(0xffffffffu, e, 24);
+    return q0 | ((q0 + q1) << 16) | ((q0 + q1 + q2) << 32) | ((q0 + q1 + q2 + q3) << 48);
+}
+
+__global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs a)
 {
     __shared__ ScanSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -130,52 +166,50 @@ __global__ void __launch_bounds__(kThreads) escape_scan_kernel(const ScanArgs a)
         const uint32_t nch = min(kRangeChunks, units - c0);
         const bool ok = sm.hdr_ok != 0;
         if (ok) {
-            // each warp counts 8 chunks; the planes of all full chunks are
-            // loaded first (24 16-byte loads in flight per lane)
-            constexpr int kPerWarp = kRangeChunks / (kThreads / 32);
+            // each warp counts 8 chunks, 2 at a time: the planes of a batch's
+            // full chunks are loaded first (6 16-byte loads in flight per lane)
+            constexpr int kBatch = 2;
             const uint8_t* base = scan_stream(a, s);
-            uint4 p[kPerWarp][3];
+#pragma unroll 1
+            for (int b = 0; b < kRangeChunks / (kThreads / 32) / kBatch; ++b) {
+                uint4 p[kBatch][3];
 #pragma unroll
-            for (int ii = 0; ii < kPerWarp; ++ii) {
-                const uint32_t i = warp + 4 * ii;
-                const uint64_t c = c0 + i;
-                if (i < nch && (c + 1) * kChunk <= a.n) {
-                    const uint4* pw = reinterpret_cast<const uint4*>(base + kHeaderBytes + c * kBlockBytes + kChunk);
+                for (int ii = 0; ii < kBatch; ++ii) {
+                    const uint32_t i = warp + 4 * (kBatch * b + ii);
+                    const uint64_t c = c0 + i;
+                    if (i < nch && (c + 1) * kChunk <= a.n) {
+                        const uint4* pw =
+                            reinterpret_cast<const uint4*>(base + kHeaderBytes + c * kBlockBytes + kChunk);
 #pragma unroll
-                    for (int qq = 0; qq < 3; ++qq) p[ii][qq] = __ldg(pw + qq * 32 + lane);
+                        for (int qq = 0; qq < 3; ++qq) p[ii][qq] = __ldg(pw + qq * 32 + lane);
+                    }
                 }
-            }
 #pragma unroll
-            for (int ii = 0; ii < kPerWarp; ++ii) {
-                const uint32_t i = warp + 4 * ii;
-                const uint64_t c = c0 + i;
-                if (i >= nch) continue;
-                uint32_t e;
-                if ((c + 1) * kChunk <= a.n) {
-                    e = __popc(~(p[ii][0].x | p[ii][1].x | p[ii][2].x)) + __popc(~(p[ii][0].y | p[ii][1].y | p[ii][2].y)) +
-                        __popc(~(p[ii][0].z | p[ii][1].z | p[ii][2].z)) + __popc(~(p[ii][0].w | p[ii][1].w | p[ii][2].w));
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-                } else {  // the stream's tail chunk
-                    e = warp_chunk_escapes(base + kHeaderBytes + c * kBlockBytes, (uint32_t)(a.n - c * kChunk));
+                for (int ii = 0; ii < kBatch; ++ii) {
+                    const uint32_t i = warp + 4 * (kBatch * b + ii);
+                    const uint64_t c = c0 + i;
+                    if (i >= nch) continue;
+                    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - c * kChunk);
+                    const uint64_t qi = warp_chunk_quarters(p[ii], base + kHeaderBytes + c * kBlockBytes, valid);
+                    if (lane == 0) sm.qinfo[i] = qi;
                 }
-                if (lane == 0) sm.cnt[i] = e;
             }
         }
         __syncthreads();
-        const uint32_t cnt = (ok && tid < (int)nch) ? sm.cnt[tid] : 0u;
+        const uint64_t qi = (ok && tid < (int)nch) ? sm.qinfo[tid] : 0ull;
+        const uint32_t cnt = chunk_escapes(qi);
         uint32_t agg;
         const uint32_t ex = block_exclusive_scan<kThreads>(cnt, sm.scan, &agg);
         if (tid < (int)nch) {
             a.local[(uint64_t)s * units + c0 + tid] = ex;
-            a.count[(uint64_t)s * units + c0 + tid] = cnt;
+            a.qinfo[(uint64_t)s * units + c0 + tid] = qi;
         }
         if (tid == 0) a.totals[r] = agg;
         __syncthreads();
     }
     pdl_launch_dependents();
     if (arrive_last(a.ctrl, &sm.last)) {
-        cta_segmented_exclusive_scan<kThreads, 8>(
+        cta_segmented_exclusive_scan<kThreads, 4>(
             a.totals, a.bases, nr, [&](uint32_t r) { return r % rps == 0; }, sm.scan64, sm.scan_f);
         __syncthreads();
         // every stream's recount must equal its header's escape count

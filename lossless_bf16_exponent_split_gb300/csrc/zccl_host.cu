@@ -31,8 +31,8 @@ struct DeviceInfo {
     int compress_per_sm_batched[13] = {};
     int scan_per_sm = 1;
     int decompress_per_sm = 1;
-    int reduce_per_sm_small = 1;  // S <= kSmallShards
-    int reduce_per_sm_large = 1;  // any S <= ZCCL_MAX_SHARDS
+    // the reduction's occupancy, [plain BF16 steps or not][S <= kSmallShards, any S <= ZCCL_MAX_SHARDS]
+    int reduce_per_sm[2][2] = {{1, 1}, {1, 1}};
 };
 constexpr uint32_t kSmallShards = 32;
 static_assert(ZCCL_MAX_SEGMENTS == 1u << 12, "one occupancy bucket per power of two up to the segment limit");
@@ -52,8 +52,10 @@ const DeviceInfo* device_info()
         for (int b = 0; b < 13; ++b) d.compress_per_sm_batched[b] = compress_ctas_per_sm(1u << b);
         d.scan_per_sm = scan_ctas_per_sm();
         d.decompress_per_sm = decompress_ctas_per_sm();
-        d.reduce_per_sm_small = reduce_ctas_per_sm(kSmallShards);
-        d.reduce_per_sm_large = reduce_ctas_per_sm(ZCCL_MAX_SHARDS);
+        for (int plain = 0; plain < 2; ++plain) {
+            d.reduce_per_sm[plain][0] = reduce_ctas_per_sm(kSmallShards, plain != 0);
+            d.reduce_per_sm[plain][1] = reduce_ctas_per_sm(ZCCL_MAX_SHARDS, plain != 0);
+        }
     });
     return &d;
 }
@@ -103,9 +105,9 @@ DecompressLayout decompress_layout(uint64_t units)
 }
 
 // Decompression / reduction workspace, per stream: escape total per range |
-// range base | chunk prefix within its range | escape count per chunk.
+// range base | chunk prefix within its range | quarter word per chunk.
 struct ScanLayout {
-    uint64_t totals, bases, local, count, total;
+    uint64_t totals, bases, local, qinfo, total;
 };
 ScanLayout scan_layout(uint64_t units, uint64_t S)
 {
@@ -114,8 +116,8 @@ ScanLayout scan_layout(uint64_t units, uint64_t S)
     l.totals = kPrefixBytes;
     l.bases = round_up(l.totals + 4 * R, 16);
     l.local = round_up(l.bases + 8 * R, 16);
-    l.count = round_up(l.local + 4 * S * units, 16);
-    l.total = round_up(l.count + 4 * S * units, 256);
+    l.qinfo = round_up(l.local + 4 * S * units, 16);
+    l.total = round_up(l.qinfo + 8 * S * units, 256);
     return l;
 }
 
@@ -327,7 +329,7 @@ zccl_status_t reduce_impl(const void* const* d_streams, const uint64_t* d_in_byt
     sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
     sc.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
     sc.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
-    sc.count = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.count);
+    sc.qinfo = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.qinfo);
     sc.status = d_status;
     ReduceArgs a{};
     a.streams = d_streams;
@@ -341,9 +343,9 @@ zccl_status_t reduce_impl(const void* const* d_streams, const uint64_t* d_in_byt
     a.ctrl = sc.ctrl;
     a.bases = sc.bases;
     a.local_off = sc.local;
-    a.count = sc.count;
+    a.qinfo = sc.qinfo;
     a.status = d_status;
-    const int per_sm = S <= kSmallShards ? dev->reduce_per_sm_small : dev->reduce_per_sm_large;
+    const int per_sm = dev->reduce_per_sm[(d_local != nullptr || accumulate) ? 1 : 0][S <= kSmallShards ? 0 : 1];
     return launch_reduce(sc, a, grid_for((uint64_t)S * ranges_of(units), dev->scan_per_sm, dev->sms),
                          grid_for(units, per_sm, dev->sms), stream) == cudaSuccess
                ? ZCCL_OK

@@ -40,7 +40,7 @@ struct ScanArgs {
     uint32_t* totals;            // [S][ranges per stream] escapes per range
     uint64_t* bases;             // [S][ranges per stream] range offset in its stream
     uint32_t* local;             // [S][units] chunk offset within its range
-    uint32_t* count;             // [S][units] escapes per chunk
+    uint64_t* qinfo;             // [S][units] quarter word per chunk (quarter_before / quarter_end)
     uint32_t* status;
 };
 
@@ -67,8 +67,8 @@ struct ReduceArgs {
     uint64_t n;
     WsCtrl* ctrl;
     uint64_t* bases;             // from the scan: [S][ranges per stream] (cleared by the last CTA)
-    uint32_t* local_off;         // [S][units] chunk prefix within its range (each cleared once read)
-    uint32_t* count;             // [S][units] (each cleared once read)
+    uint32_t* local_off;         // [S][units] chunk prefix within its range (cleared by the CTA that read it)
+    uint64_t* qinfo;             // [S][units] quarter words (cleared by the CTA that read them)
     uint32_t* status;
 };
 
@@ -127,7 +127,7 @@ int decompress_ctas_per_sm();
 
 cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
                           cudaStream_t stream);
-int reduce_ctas_per_sm(uint32_t S);
+int reduce_ctas_per_sm(uint32_t S, bool plain);
 
 cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint64_t* hist, bool accumulate, int sms,
                              cudaStream_t stream);

@@ -10,17 +10,37 @@
 // add an IEEE fp32 add (no FMA, no flush to zero) in shard order, x_s decoded
 // from stream s; a NaN sum becomes 0x7FC0.
 //
-// GB300 design: the escape scan kernel (zccl_decompress.cu) first computes
-// every shard's per-chunk zero-point offsets (range base + prefix within the
-// range) from the code planes; then,
-// started by programmatic dependent launch, reduce_kernel walks the chunks
-// (persistent grid, static stride) and, for each chunk, the S shard blocks
-// in order through a 3-stage ring of shared buffers: each step is one TMA
-// bulk copy of the shard's block plus one of its zero-point run, so two
-// steps are in flight while one decodes.  Each thread decodes 32 elements of
-// the step straight into fp32 accumulators held in registers; after the
-// last shard it rounds and stores 16-byte vectors.  Every compressed byte is
-// read once and the BF16 result written once.
+// GB300 design: the escape scan kernel (zccl_decompress.cu) first computes,
+// for every shard and chunk, the chunk's zero-point offset (range base +
+// prefix within the range) and the escapes before each quarter of the chunk
+// (1024 slots).  Then, started by programmatic dependent launch,
+// reduce_kernel hands each warp one chunk quarter at a time: the four warps
+// of a CTA take the four quarters of the CTA's chunks (static stride over
+// the chunks).  A warp walks the S shards of its quarter in order through
+// its own 3-stage ring of shared buffers, which its lanes fill themselves
+// with 16-byte asynchronous copies (cp.async): each lane the 32
+// sign-mantissa bytes it decodes, 24 lanes the quarter's 128 bytes of each
+// code plane, and as many lanes as needed the 16-byte aligned cover of the
+// quarter's run of the zero-point array.  A step waits for its own copies
+// (cp.async.wait_group) and then for the warp's (a warp barrier).  No warp
+// ever waits for another, and no single thread issues copies for others.
+// Lane l owns slots [32 l, 32 l + 32) of the quarter, i.e. one word of each
+// code plane: after a warp scan of the escape counts it places its own
+// escaped exponents, then decodes its 32 elements straight into fp32 sums
+// held in registers.  After the last shard it rounds and stores them.
+// Every compressed byte is read once and the BF16 result written once.
+//
+// Shared-memory accesses are laid out so that no bank is hit twice by one
+// instruction: a lane's 32 sign-mantissa bytes are read as two 16-byte
+// halves in an order that alternates with bit 2 of the lane, and its
+// escaped exponents are stored in 8-byte groups whose order is XOR-swizzled
+// with bits 2..3 of the lane.  The code-plane words are read one per lane.
+//
+// The fold starts every chunk from -0.0: -0.0 + x == x exactly for every
+// fp32 x (including +0, -0, subnormals, infinities and NaN), so every shard,
+// the first included, is one add and no step needs a separate first form.
+// The adds widen BF16 to fp32 inside the add instruction (exact), so a
+// packed pair of BF16 values feeds two adds with no unpacking.
 #include <cstdint>
 
 #include "zccl_common.cuh"
@@ -31,48 +51,57 @@ namespace zccl {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 3;
-// Shared memory (three stages, about 35 KB) admits 6 CTAs per SM; registers
-// are capped to match, so neither instance falls below it.
+constexpr uint32_t kQuarter = kChunk / 4;          // slots of one warp's share of a chunk
+constexpr uint32_t kStageBytes = 2 * kQuarter;     // a quarter of plain BF16, or its block part + zero points
+constexpr uint32_t kPlaneOff = kQuarter;           // after the sign-mantissa bytes: 3 planes of 128 bytes
+constexpr uint32_t kPlaneBytes = kQuarter / 8;
+constexpr uint32_t kZpOff = kQuarter + 3 * kPlaneBytes;
+constexpr uint32_t kZpCap = 512;                   // one 16-byte copy per lane: the cover of up to 482 escapes
+// Shared memory (about 35 KB) admits 6 CTAs per SM; registers are capped
+// to match.
 constexpr int kCtasPerSm = 6;
+static_assert(kZpOff % 16 == 0 && kZpOff + kZpCap <= kStageBytes, "the zero-point cover fits the stage");
 
-// One stage of the ring: a shard's block and its zero-point run, or a chunk
-// of plain BF16 (the rank's own shard, or the output being accumulated into).
-struct __align__(16) Stage {
-    uint8_t blk[kBlockBytes];
-    uint8_t zpb[kZpBufBytes];
-};
-static_assert(sizeof(Stage) >= 2 * kChunk, "a chunk of plain BF16 fits a stage");
-
-struct __align__(16) ReduceSmem {
-    Stage stage[kStages];
-    uint8_t expo[kChunk];
-    uint64_t bar[kStages];
-    uint32_t zdelta[kStages];
-    uint32_t zcount[kStages];
-    uint32_t scan[2][kThreads / 32];  // the warps' escape totals, by step parity
-    uint32_t abort;
+struct __align__(128) ReduceSmem {
+    uint8_t stage[kWarps][kStages][kStageBytes];
+    uint8_t xe[kWarps][kQuarter];  // each lane's escaped exponents (rotated), 32 bytes
+    uint32_t spread[3][256];       // spread_nibbles(b) << p, p = plane
+    // per warp, two windows of 32 steps: the quarter's first zero-point
+    // offset and its escape count
+    uint64_t win[kWarps][2 * 32][2];
     uint32_t last;
-    uint32_t spread[256];  // spread_nibbles of every byte
 };
-// followed by per-shard tables: const uint8_t* base[S]; uint64_t n_esc[S]; uint32_t lut[S][2]
+// followed by per-shard tables: blk[S], zpa[S], n_esc[S] (8 bytes each), lut[S] (uint2)
 
+// Per shard: where its chunk blocks and its zero-point array start, its
+// escape count, and its LUT with every exponent rotated right by one bit
+// (entry c <-> code c; entry 0, code 000, unused).
 struct ShardTables {
-    const uint8_t** base;
+    const uint8_t** blk;
+    const uint8_t** zpa;
     uint64_t* n_esc;
-    uint32_t* lut;
+    uint2* lut;
 };
 
 __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t S)
 {
     ShardTables t;
     uint8_t* p = smem_raw + sizeof(ReduceSmem);
-    t.base = reinterpret_cast<const uint8_t**>(p);
-    t.n_esc = reinterpret_cast<uint64_t*>(p + 8ull * S);
-    t.lut = reinterpret_cast<uint32_t*>(p + 16ull * S);
+    t.blk = reinterpret_cast<const uint8_t**>(p);
+    t.zpa = reinterpret_cast<const uint8_t**>(p + 8ull * S);
+    t.n_esc = reinterpret_cast<uint64_t*>(p + 16ull * S);
+    t.lut = reinterpret_cast<uint2*>(p + 24ull * S);
     return t;
 }
+
+// An exponent byte rotated right by one bit: bit 7 = exponent bit 0, bits
+// 0..6 = exponent >> 1 -- the low and high byte of a BF16 value then each
+// take one masked merge with the sign-mantissa byte.
+__device__ __forceinline__ uint32_t rot_exp(uint32_t e) { return ((e >> 1) | (e << 7)) & 0xFFu; }
+__device__ __forceinline__ uint32_t rot_exp4(uint32_t w) { return ((w >> 1) & 0x7F7F7F7Fu) | ((w << 7) & 0x80808080u); }
 
 // The steps of an output chunk: (accumulating) the output's current values,
 // then the S inputs in rank order -- each a shard's compressed stream, or
@@ -103,246 +132,302 @@ __device__ __forceinline__ uint32_t step_kind(const ReduceArgs& a, uint32_t q, u
     return (a.local != nullptr && q == a.local_pos) ? kStepLocal : kStepStream;
 }
 
-// Offsets of one stream step's zero-point run: the range base plus the
-// chunk's prefix within its range, and its escape count (loaded one
-// iteration ahead of their use by issue_step, so thread 0 never waits on
-// them).
-struct StepOffsets {
-    uint64_t base;
-    uint32_t local, count;
-};
-
-template <bool kPlain>
-__device__ __forceinline__ StepOffsets load_offsets(const ReduceArgs& a, uint32_t c, uint32_t q, uint32_t total)
+// acc += the two BF16 values packed in w (low half to .x, high half to
+// .y): each an fp32 add of the exactly widened BF16 value, rounded to
+// nearest even, no flush to zero.
+__device__ __forceinline__ void add_bf16x2(float2& acc, uint32_t w)
 {
-    StepOffsets o{0, 0, 0};
-    uint32_t s = 0;
-    if (c >= total || step_kind<kPlain>(a, q, &s) != kStepStream) return o;
-    const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
-    const uint64_t idx = (uint64_t)s * total + c;
-    o.base = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks);
-    o.local = __ldcg(a.local_off + idx);
-    o.count = __ldcg(a.count + idx);
-    return o;
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n add.rn.f32.bf16 %1, hi, %1;\n}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "r"(w));
 }
 
-// Thread 0: queue step q of chunk c into stage st.
-template <bool kPlain>
-__device__ __forceinline__ void issue_step(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t c,
-                                           uint32_t q, int st, uint32_t total, const StepOffsets& off)
+// Adds 8 BF16 values (packed in pairs) to four fp32 pairs.
+__device__ __forceinline__ void add8(float2* acc, uint4 o)
 {
-    if (c >= total) return;
-    uint32_t s = 0;
-    const uint32_t kind = step_kind<kPlain>(a, q, &s);
-    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - (uint64_t)c * kChunk);
-    if (kind != kStepStream) {  // plain BF16: whole 16-byte pieces by bulk copy, the rest by plain loads
-        const uint16_t* src = (kind == kStepLocal ? a.local : a.out) + (uint64_t)c * kChunk;
-        const uint32_t bytes = (valid * 2) & ~15u;
-        mbar_arrive_expect_tx(&sm.bar[st], bytes);
-        if (bytes) bulk_g2s(sm.stage[st].blk, src, bytes, &sm.bar[st]);
-        return;
-    }
-    const uint32_t bytes = slots_of(valid) * 11 / 8;
-    const uint64_t o0 = off.base + off.local;
-    const uint64_t o1 = o0 + off.count;
-    uint32_t zbytes = 0, delta = 0, cnt = 0;
-    const uint64_t zp = zp_offset_of(a.n);
-    if (o1 <= t.n_esc[s] && o1 - o0 <= kChunk) {
-        cnt = (uint32_t)(o1 - o0);
-        if (cnt) {
-            const uint64_t lo = zp + o0, lo16 = lo & ~15ull, hi16 = round_up(zp + o1, 16);
-            zbytes = (uint32_t)(hi16 - lo16);
-            delta = (uint32_t)(lo - lo16);
-        }
-    } else {
-        report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-    }
-    sm.zdelta[st] = delta;
-    sm.zcount[st] = cnt;
-    mbar_arrive_expect_tx(&sm.bar[st], bytes + zbytes);
-    bulk_g2s(sm.stage[st].blk, t.base[s] + kHeaderBytes + (uint64_t)c * kBlockBytes, bytes, &sm.bar[st]);
-    if (zbytes) bulk_g2s(sm.stage[st].zpb, t.base[s] + ((zp + o0) & ~15ull), zbytes, &sm.bar[st]);
+    add_bf16x2(acc[0], o.x);
+    add_bf16x2(acc[1], o.y);
+    add_bf16x2(acc[2], o.z);
+    add_bf16x2(acc[3], o.w);
 }
 
-// One step's share of a thread: decode (or read) its 32 elements of the
-// stage and add them to its accumulators.  kFull: the chunk is whole, so
-// no element needs a bound check and the four groups interleave freely.
-template <bool kFull>
-__device__ __forceinline__ void fold_step(const uint8_t* blk, uint32_t L, uint32_t kind, uint32_t lut_lo,
-                                          uint32_t lut_hi, const ReduceSmem& sm, float2 (&acc)[16], bool first_step)
+// Two fp32 sums -> a packed pair of BF16 values (lo in the low half), each
+// rounded to nearest, ties to even, by the conversion instruction.  A NaN
+// comes out as some NaN; canonical_nan makes it 0x7FC0.
+__device__ __forceinline__ uint32_t pack_rne(float lo, float hi)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (kFull) L = kChunk;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-        if (kFull || e0 < L) {
-            const uint4 o = kind == kStepStream
-                                ? decode8(*reinterpret_cast<const uint2*>(blk + e0), blk[L + (e0 >> 3)],
-                                          blk[L + L / 8 + (e0 >> 3)], blk[L + L / 4 + (e0 >> 3)], lut_lo, lut_hi,
-                                          *reinterpret_cast<const uint2*>(sm.expo + e0), sm.spread)
-                                : *reinterpret_cast<const uint4*>(blk + 2 * e0);
-            const uint32_t w[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-                acc[4 * i + k] = first_step ? f : __fadd2_rn(acc[4 * i + k], f);
-            }
-        }
-    }
+    uint32_t w;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+    return w;
+}
+// Bit 15 (31) set where the low (high) half of a BF16 pair is a NaN:
+// |v| > 0x7F80 in each half, by one add that cannot carry across halves.
+__device__ __forceinline__ uint32_t nan_halves(uint32_t w) { return ((w & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u; }
+__device__ __forceinline__ uint32_t canonical_nan(uint32_t w)
+{
+    const uint32_t m = ((nan_halves(w) >> 15) & 0x00010001u) * 0xFFFFu;
+    return (w & ~m) | (0x7FC07FC0u & m);
 }
 
-// All threads of the CTA: the CTA's chunks (static stride), each over its
-// steps in order.  The fp32 sums are kept as pairs and added with the
-// two-lane add (each lane rounds to nearest even exactly as a scalar add).
-template <bool kPlain>
-__device__ __forceinline__ void reduce_chunks(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
+// Decodes 8 elements and adds them to four fp32 pairs: N their code
+// nibbles, smb their sign-mantissa bytes, xe their escaped exponents
+// (rotated; bytes of other elements are ignored), lut the rotated LUT.
+__device__ __forceinline__ void decode_add8(float2* acc, uint32_t N, uint2 smb, uint2 lut, uint2 xe)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t e_lo = __byte_perm(lut.x, lut.y, N);      // nibble k of N selects byte k
+    uint32_t e_hi = __byte_perm(lut.x, lut.y, N >> 16);
+    const uint32_t m_lo = __byte_perm(0xFFu, 0u, N);   // 0xFF where the code is 000
+    const uint32_t m_hi = __byte_perm(0xFFu, 0u, N >> 16);
+    e_lo = (e_lo & ~m_lo) | (xe.x & m_lo);
+    e_hi = (e_hi & ~m_hi) | (xe.y & m_hi);
+    // low byte = exponent bit 0 << 7 | mantissa; high byte = sign << 7 | exponent >> 1
+    const uint32_t lo_a = (e_lo & 0x80808080u) | (smb.x & 0x7F7F7F7Fu);
+    const uint32_t hi_a = (smb.x & 0x80808080u) | (e_lo & 0x7F7F7F7Fu);
+    const uint32_t lo_b = (e_hi & 0x80808080u) | (smb.y & 0x7F7F7F7Fu);
+    const uint32_t hi_b = (smb.y & 0x80808080u) | (e_hi & 0x7F7F7F7Fu);
+    add_bf16x2(acc[0], __byte_perm(lo_a, hi_a, 0x5140));
+    add_bf16x2(acc[1], __byte_perm(lo_a, hi_a, 0x7362));
+    add_bf16x2(acc[2], __byte_perm(lo_b, hi_b, 0x5140));
+    add_bf16x2(acc[3], __byte_perm(lo_b, hi_b, 0x7362));
+}
+
+// One warp: the zero-point offset and escape count of its quarter in steps
+// w .. w + 31 (lane i: step w + i) into window slot (w / 32) & 1 of the
+// warp.  The loads are waited for here: it happens once per 32 steps.
+template <bool kPlain>
+__device__ __forceinline__ void load_window(const ReduceArgs& a, ReduceSmem& sm, uint32_t w, uint32_t steps)
+{
+    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5, step = w + lane;
     const uint32_t total = (uint32_t)units_of(a.n);
     const uint32_t Q = steps_per_chunk<kPlain>(a);
-    // thread 0: `ahead` holds the offsets of the next step to queue, at
-    // (ic, iq); (pc, pq) is the step after it
-    StepOffsets ahead{0, 0, 0};
-    uint32_t pc = blockIdx.x, pq = 0, ic = 0, iq = 0;
-    auto advance = [&]() {
-        if (++pq == Q) {
-            pq = 0;
-            pc += gridDim.x;
+    uint64_t zq = 0, cnt = 0;
+    if (step < steps) {
+        const uint32_t k = step / Q, sq = step - k * Q;
+        uint32_t s = 0;
+        if (step_kind<kPlain>(a, sq, &s) == kStepStream) {
+            const uint64_t c = blockIdx.x + (uint64_t)k * gridDim.x;
+            const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
+            const uint64_t qi = __ldcg(a.qinfo + (uint64_t)s * total + c);
+            const uint32_t before = quarter_before(qi, q);
+            zq = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks) +
+                 __ldcg(a.local_off + (uint64_t)s * total + c) + before;
+            cnt = quarter_end(qi, q) - before;
         }
-    };
-    if (tid == 0) {
-        for (int j = 0; j + 1 < kStages; ++j) {
-            issue_step<kPlain>(a, sm, t, pc, pq, j, total, load_offsets<kPlain>(a, pc, pq, total));
-            advance();
-        }
-        ic = pc;
-        iq = pq;
-        ahead = load_offsets<kPlain>(a, pc, pq, total);
-        advance();
     }
+    const uint32_t e = smem_addr(sm.win[q][((w / 32) & 1) * 32 + lane]);
+    sts_u64(e, zq);
+    sts_u64(e + 8, cnt);
+}
+
+// One warp: its quarter q of the CTA's chunks blockIdx.x + k * gridDim.x,
+// each over its steps in order.  The fp32 sums are kept as pairs.
+template <bool kPlain>
+__device__ __forceinline__ void reduce_quarters(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t)
+{
+    const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const uint32_t total = (uint32_t)units_of(a.n);
+    const uint32_t Q = steps_per_chunk<kPlain>(a);
+    const uint32_t G = gridDim.x;
+    const uint32_t tab = smem_addr(t.blk);
+    const uint32_t S = a.S;
+    auto unit_valid = [&](uint32_t k) -> uint32_t {
+        return (uint32_t)min((uint64_t)kChunk, a.n - (blockIdx.x + (uint64_t)k * G) * kChunk);
+    };
+    // this warp's chunks; the tail chunk may have no slots in quarter q
+    uint32_t units = 0;
+    if (blockIdx.x < total) {
+        units = (total - 1 - blockIdx.x) / G + 1;
+        if (q * kQuarter >= slots_of(unit_valid(units - 1))) --units;
+    }
+    const uint32_t steps = units * Q;
+    const uint32_t stage0 = smem_addr(sm.stage[q][0]);
+
+    load_window<kPlain>(a, sm, 0, steps);
+    load_window<kPlain>(a, sm, 32, steps);
+    __syncwarp();
+
+    // Issue cursor: step ij, unit ik, step is within it, into stage ist.
+    // Every lane copies; each step is one cp.async group of every lane
+    // (empty past the last step, so that the group count stays uniform).
+    uint32_t ij = 0, ik = 0, is = 0, ist = 0;
+    auto issue = [&]() {
+        if (ij < steps) {
+            // mid-window: the next window (its slot held steps all consumed by now)
+            if ((ij & 31) == 16) {
+                load_window<kPlain>(a, sm, (ij & ~31u) + 32, steps);
+                __syncwarp();
+            }
+            const uint64_t c = blockIdx.x + (uint64_t)ik * G;
+            const uint32_t valid = unit_valid(ik);
+            const uint32_t dst = stage0 + ist * kStageBytes;
+            uint32_t s = 0;
+            const uint32_t kind = step_kind<kPlain>(a, is, &s);
+            if (kind != kStepStream) {  // plain BF16: the lane's whole 16-byte pieces, the rest by plain loads
+                const uint32_t vq = min(kQuarter, valid - q * kQuarter);
+                const uint16_t* src = (kind == kStepLocal ? a.local : a.out) + c * kChunk + q * kQuarter;
+#pragma unroll
+                for (uint32_t k = 0; k < 4; ++k) {
+                    const uint32_t e0 = 32 * lane + 8 * k;  // the piece's first element
+                    if (e0 + 8 <= vq) cp_async16(dst + 2 * e0, src + e0);
+                }
+            } else {
+                const uint32_t L = slots_of(valid);
+                const uint8_t* blk = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * s)) + c * kBlockBytes;
+                // the lane's sign-mantissa bytes
+                cp_async16(dst + 32 * lane, blk + q * kQuarter + 32 * lane);
+                cp_async16(dst + 32 * lane + 16, blk + q * kQuarter + 32 * lane + 16);
+                // lanes 0..23: 16 bytes of plane lane / 8
+                if (lane < 24) {
+                    const uint32_t p = lane >> 3, piece = 16 * (lane & 7);
+                    cp_async16(dst + kPlaneOff + p * kPlaneBytes + piece, blk + L + p * (L / 8) + q * kPlaneBytes + piece);
+                }
+                // the quarter's zero points: its 16-byte aligned cover, one piece per lane
+                const uint32_t wa = smem_addr(sm.win[q][ij & 63]);
+                const uint64_t zq = lds_u64w(wa);
+                const uint32_t cnt = (uint32_t)lds_u64w(wa + 8);
+                const bool ok = cnt <= kQuarter && zq + cnt <= lds_u64w(tab + 16 * S + 8 * s);
+                const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * S + 8 * s)) + zq;
+                const uint32_t zmis = (uint32_t)(uintptr_t)zsrc & 15u;
+                const uint32_t cover = (zmis + cnt + 15u) & ~15u;
+                if (ok && cover <= kZpCap && 16 * lane < cover) cp_async16(dst + kZpOff + 16 * lane, zsrc - zmis + 16 * lane);
+            }
+            ++ij;
+            if (++is == Q) {
+                is = 0;
+                ++ik;
+            }
+            if (++ist == kStages) ist = 0;
+        }
+        cp_async_commit();
+    };
+    for (int i = 0; i + 1 < kStages; ++i) issue();
+
+    // lane constants of the conflict-free layouts
+    const uint32_t h = (lane >> 2) & 1;            // which 16-byte half of its bytes the lane reads first
+    const uint32_t x = (2 * h) ^ (lane >> 2 & 3);  // processing group i <-> swizzled escape group i ^ x
+    const uint32_t xa = smem_addr(sm.xe[q] + 32 * lane);  // the lane's escaped exponents
+    const uint32_t xsw = 8 * (lane >> 2 & 3);      // escape byte of element b sits at xa + (b ^ xsw)
+    const uint32_t sp = smem_addr(sm.spread[0]);
+    const uint32_t lut0 = tab + 24 * S;
 
     float2 acc[16];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) acc[q] = make_float2(0.0f, 0.0f);
+    for (int k = 0; k < 16; ++k) acc[k] = make_float2(-0.0f, -0.0f);
 
-    uint32_t j = 0, q = 0, c = blockIdx.x;  // step, its place in the chunk's steps, its chunk
-    for (;; ++j) {
-        if (c >= total) break;
-        const int st = j % kStages;
-        uint32_t s = 0;
-        const uint32_t kind = step_kind<kPlain>(a, q, &s);
-        const uint64_t first = (uint64_t)c * kChunk;
-        const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - first);
-        const uint32_t L = slots_of(valid);
-        if (!mbar_wait(&sm.bar[st], (j / kStages) & 1)) atomicExch(&sm.abort, 1u);
-        uint8_t* blk = sm.stage[st].blk;
-        uint32_t esc = 0, incl = 0;
-        if (kind != kStepStream) {  // plain BF16: the last < 8 values by plain loads
-            const uint32_t done = valid & ~7u;
-            if (tid < (int)(valid - done)) {
-                const uint16_t* src = kind == kStepLocal ? a.local : a.out;
-                reinterpret_cast<uint16_t*>(blk)[done + tid] = src[first + done + tid];
-            }
-        } else {
-            if (tid < (int)(L / 32)) {
-                const uint32_t* pw = reinterpret_cast<const uint32_t*>(blk + L);
-                const uint32_t w0 = 32u * tid;
-                const uint32_t vmask = w0 + 32 <= valid ? 0xFFFFFFFFu
-                                       : (w0 >= valid ? 0u : ((1u << (valid - w0)) - 1u));
-                esc = ~(pw[tid] | pw[L / 32 + tid] | pw[L / 16 + tid]) & vmask;
-            }
-            incl = __popc(esc);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) sm.scan[j & 1][warp] = incl;
-        }
-        // the step's one barrier: stage st has landed for every thread, the
-        // warps' escape totals are posted, and every thread is past step
-        // j - 1, so its stage is free (a warp reaches the next step's
-        // totals, in the other parity's slots, only through this barrier)
-        __syncthreads();
-        if (sm.abort) {
-            if (tid == 0) report(a.status, ZCCL_ERR_TIMEOUT);
-            break;
-        }
-        // refill the freed stage with step j + kStages - 1
-        if (tid == 0) {
-            issue_step<kPlain>(a, sm, t, ic, iq, (j + kStages - 1) % kStages, total, ahead);
-            ic = pc;
-            iq = pq;
-            ahead = load_offsets<kPlain>(a, pc, pq, total);
-            advance();
-        }
-        if (kind == kStepStream) {
-            uint32_t before = 0, agg = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
-                const uint32_t v = sm.scan[j & 1][w];
-                before += w < warp ? v : 0u;
-                agg += v;
-            }
-            if (agg == sm.zcount[st]) {
-                const uint8_t* src = sm.stage[st].zpb + sm.zdelta[st] + before + incl - __popc(esc);
-                uint32_t m = esc, jj = 0;
-                while (m) {
-                    const uint32_t b = __ffs(m) - 1;
-                    m &= m - 1;
-                    sm.expo[32u * tid + b] = src[jj++];
-                }
-            } else if (tid == 0) {
-                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            }
-            // warp w folds elements [1024w, 1024w + 1024): its own lanes'
-            // escape words, so the warp placed its exponents itself
+    uint32_t cst = 0, j = 0;  // consume cursor: stage, step
+    for (uint32_t k = 0; k < units; ++k) {
+        const uint64_t c = blockIdx.x + (uint64_t)k * G;
+        const uint32_t valid = unit_valid(k);
+        const uint32_t vq = min(kQuarter, valid - q * kQuarter);
+        const uint32_t e0 = 32 * lane;
+        const uint32_t vmask = e0 + 32 <= vq ? 0xFFFFFFFFu : (e0 >= vq ? 0u : ((1u << (vq - e0)) - 1u));
+        for (uint32_t sq = 0; sq < Q; ++sq, ++j) {
+            // every lane is past step j - 1: refill its stage with step j + kStages - 1
             __syncwarp();
-        }
-        const uint32_t lut_lo = t.lut[2 * s], lut_hi = t.lut[2 * s + 1];
-        if (L == kChunk) {
-            fold_step<true>(blk, L, kind, lut_lo, lut_hi, sm, acc, q == 0);
-        } else {
-            fold_step<false>(blk, L, kind, lut_lo, lut_hi, sm, acc, q == 0);
-        }
-        if (q + 1 == Q) {
-            // the chunk's offset words have had their one reader (loaded
-            // steps ago): clear them
-            for (uint32_t r = tid; r < a.S; r += kThreads) {
-                a.local_off[(uint64_t)r * total + c] = 0;
-                a.count[(uint64_t)r * total + c] = 0;
-            }
-            uint16_t* dst = a.out + first;
+            issue();
+            cp_async_wait<kStages - 1>();  // this lane's copies of step j
+            __syncwarp();                  // ... and every lane's
+            const uint32_t stg = stage0 + cst * kStageBytes;
+            uint32_t s = 0;
+            const uint32_t kind = step_kind<kPlain>(a, sq, &s);
+            if (kind == kStepStream) {
+                const uint32_t P0 = lds_u32(stg + kPlaneOff + 4 * lane);
+                const uint32_t P1 = lds_u32(stg + kPlaneOff + kPlaneBytes + 4 * lane);
+                const uint32_t P2 = lds_u32(stg + kPlaneOff + 2 * kPlaneBytes + 4 * lane);
+                const uint4 A = lds_u128(stg + 32 * lane + 16 * h);
+                const uint4 B = lds_u128(stg + 32 * lane + 16 * (h ^ 1));
+                const uint32_t esc = ~(P0 | P1 | P2) & vmask;
+                const uint32_t ne = __popc(esc);
+                uint32_t incl = ne;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t e0 = 1024u * warp + 256u * i + 8u * lane;
-                if (e0 >= valid) continue;
-                uint4 o;
-                o.x = rne_bf16(acc[4 * i + 0].x) | (rne_bf16(acc[4 * i + 0].y) << 16);
-                o.y = rne_bf16(acc[4 * i + 1].x) | (rne_bf16(acc[4 * i + 1].y) << 16);
-                o.z = rne_bf16(acc[4 * i + 2].x) | (rne_bf16(acc[4 * i + 2].y) << 16);
-                o.w = rne_bf16(acc[4 * i + 3].x) | (rne_bf16(acc[4 * i + 3].y) << 16);
-                if (e0 + 8 <= valid) {
-                    *reinterpret_cast<uint4*>(dst + e0) = o;
-                } else {
-                    store_partial(dst + e0, o, valid - e0);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= (uint32_t)o) incl += y;
                 }
+                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+                const uint32_t wa = smem_addr(sm.win[q][j & 63]);
+                const uint64_t zq = lds_u64w(wa);
+                const uint32_t cnt = (uint32_t)lds_u64w(wa + 8);
+                const bool ok = cnt <= kQuarter && zq + cnt <= lds_u64w(tab + 16 * S + 8 * s);
+                if (ok && tot == cnt) {
+                    if (esc) {
+                        const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * S + 8 * s)) + zq;
+                        const uint32_t zmis = (uint32_t)(uintptr_t)zsrc & 15u;
+                        uint32_t m = esc;
+                        if (((zmis + cnt + 15u) & ~15u) <= kZpCap) {  // the run is in the stage
+                            const uint32_t src = stg + kZpOff + zmis + (incl - ne);
+                            for (uint32_t r = 0; m; ++r) {
+                                const uint32_t b = __ffs(m) - 1;
+                                m &= m - 1;
+                                sts_u8(xa + (b ^ xsw), rot_exp(lds_u8(src + r)));
+                            }
+                        } else {  // a run too long for the stage: read in place
+                            const uint8_t* src = zsrc + (incl - ne);
+                            for (uint32_t r = 0; m; ++r) {
+                                const uint32_t b = __ffs(m) - 1;
+                                m &= m - 1;
+                                sts_u8(xa + (b ^ xsw), rot_exp(__ldg(src + r)));
+                            }
+                        }
+                    }
+                } else if (lane == 0) {
+                    report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+                }
+                const uint2 lut = lds_u64(lut0 + 8 * s);
+                // planes rotated so that processing group i is byte i of each word
+                const uint32_t R0 = __funnelshift_r(P0, P0, 16 * h);
+                const uint32_t R1 = __funnelshift_r(P1, P1, 16 * h);
+                const uint32_t R2 = __funnelshift_r(P2, P2, 16 * h);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t N = lds_u32(sp + 4 * ((R0 >> (8 * i)) & 0xFF)) |
+                                       lds_u32(sp + 1024 + 4 * ((R1 >> (8 * i)) & 0xFF)) |
+                                       lds_u32(sp + 2048 + 4 * ((R2 >> (8 * i)) & 0xFF));
+                    const uint2 xe = lds_u64(xa + 8 * (i ^ x));
+                    const uint2 smb = i == 0 ? make_uint2(A.x, A.y)
+                                      : i == 1 ? make_uint2(A.z, A.w)
+                                      : i == 2 ? make_uint2(B.x, B.y)
+                                               : make_uint2(B.z, B.w);
+                    decode_add8(&acc[4 * i], N, smb, lut, xe);
+                }
+            } else {  // plain BF16: the last vq % 8 values by plain loads
+                const uint32_t done = vq & ~7u;
+                if (lane < vq - done) {
+                    const uint16_t* src = kind == kStepLocal ? a.local : a.out;
+                    reinterpret_cast<uint16_t*>(sm.stage[q][cst])[done + lane] = src[c * kChunk + q * kQuarter + done + lane];
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) add8(&acc[4 * i], lds_u128(stg + 64 * lane + 16 * (i ^ (2 * h))));
+            }
+            if (++cst == kStages) cst = 0;
+        }
+        // the quarter is complete: round, store, start the next one
+        uint32_t w[16];
+        uint32_t nan = 0;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            w[kk] = pack_rne(acc[kk].x, acc[kk].y);
+            nan |= nan_halves(w[kk]);
+            acc[kk] = make_float2(-0.0f, -0.0f);
+        }
+        if (__any_sync(0xffffffffu, nan != 0)) {
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) w[kk] = canonical_nan(w[kk]);
+        }
+        uint16_t* dst = a.out + c * kChunk + q * kQuarter;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t e = 32 * lane + 8 * (i ^ (2 * h));
+            const uint4 o = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            if (e + 8 <= vq) {
+                *reinterpret_cast<uint4*>(dst + e) = o;
+            } else if (e < vq) {
+                store_partial(dst + e, o, vq - e);
             }
         }
-        if (++q == Q) {  // the next chunk's first step
-            q = 0;
-            c += gridDim.x;
-        }
     }
-    // steps still in flight after an early stop at step j: j + 1 .. j + kStages - 2
-    // (step j + kStages - 1 is issued only after step j's barrier); wait for
-    // them (bounded)
-    if (tid == 0 && sm.abort) {
-        for (uint32_t jj = j + 1; jj + 1 < j + kStages; ++jj) {
-            if (blockIdx.x + (jj / Q) * gridDim.x < total) mbar_wait(&sm.bar[jj % kStages], (jj / kStages) & 1);
-        }
-    }
+    cp_async_wait<0>();  // nothing in flight when the warp leaves
 }
 
 template <bool kPlain>
@@ -359,9 +444,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const Redu
     bool ok = true;
     for (uint32_t s = tid; s < a.S; s += kThreads) {
         if (a.local != nullptr && s == a.local_pos) {  // the plain BF16 input: no stream
-            t.base[s] = nullptr;
+            t.blk[s] = nullptr;
+            t.zpa[s] = nullptr;
             t.n_esc[s] = 0;
-            t.lut[2 * s] = t.lut[2 * s + 1] = 0;
+            t.lut[s] = make_uint2(0, 0);
             continue;
         }
         const uint8_t* base = reinterpret_cast<const uint8_t*>(a.streams[s]);
@@ -375,28 +461,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const Redu
             good = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
                    zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
             t.n_esc[s] = n_esc;
-            t.lut[2 * s] = h[6] << 8;
-            t.lut[2 * s + 1] = (h[6] >> 24) | (h[7] << 8);
+            // LUT bytes, rotated: entry 0 (code 000) unused, entry c = exponent of code c
+            t.lut[s] = make_uint2(rot_exp4(h[6] << 8), rot_exp4((h[6] >> 24) | (h[7] << 8)));
         }
-        t.base[s] = base;
+        t.blk[s] = base + kHeaderBytes;
+        t.zpa[s] = base + zp_offset_of(a.n);
         ok = ok && good;
     }
-    for (uint32_t b = tid; b < 256; b += kThreads) sm.spread[b] = spread_nibbles(b);
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&sm.bar[i], 1);
-        fence_mbar_init();
-        sm.abort = 0;
+    for (uint32_t b = tid; b < 256; b += kThreads) {
+        const uint32_t v = spread_nibbles(b);
+        sm.spread[0][b] = v;
+        sm.spread[1][b] = v << 1;
+        sm.spread[2][b] = v << 2;
     }
     pdl_wait();  // offsets of the scan kernel
-    if (__syncthreads_and(ok)) {
-        reduce_chunks<kPlain>(a, sm, t);
-    } else {  // a bad header: nothing to decode, but leave the scratch clear
-        for (uint32_t c = blockIdx.x; c < total; c += gridDim.x)
-            for (uint32_t s = tid; s < a.S; s += kThreads) {
-                a.local_off[(uint64_t)s * total + c] = 0;
-                a.count[(uint64_t)s * total + c] = 0;
-            }
-    }
+    if (__syncthreads_and(ok)) reduce_quarters<kPlain>(a, sm, t);
+    // every warp of the CTA is past its last read of the offset words: clear
+    // those of the CTA's chunks (no other CTA reads them)
+    __syncthreads();
+    for (uint32_t c = blockIdx.x; c < total; c += gridDim.x)
+        for (uint32_t s = tid; s < a.S; s += kThreads) {
+            a.local_off[(uint64_t)s * total + c] = 0;
+            a.qinfo[(uint64_t)s * total + c] = 0;
+        }
     // the last CTA to finish clears the range bases: the workspace is left
     // all zero past its control block and flag area
     if (arrive_last(a.ctrl, &sm.last)) {
@@ -407,13 +494,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const Redu
 
 }  // namespace
 
-static size_t reduce_smem_bytes(uint32_t S) { return sizeof(ReduceSmem) + 24ull * S; }
+template <bool kPlain>
+static size_t reduce_smem_bytes(uint32_t S) { return sizeof(ReduceSmem) + 32ull * S; }
 
 cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_scan, uint32_t grid,
                           cudaStream_t stream)
 {
-    const size_t smem = reduce_smem_bytes(a.S);
     const bool plain = a.local != nullptr || a.accumulate;
+    const size_t smem = plain ? reduce_smem_bytes<true>(a.S) : reduce_smem_bytes<false>(a.S);
     cudaError_t e = plain ? cudaFuncSetAttribute(reduce_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem)
                           : cudaFuncSetAttribute(reduce_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -426,8 +514,9 @@ cudaError_t launch_reduce(const ScanArgs& s, const ReduceArgs& a, uint32_t grid_
 }
 
 template <bool kPlain>
-static int reduce_occupancy(size_t smem)
+static int reduce_occupancy(uint32_t S)
 {
+    const size_t smem = reduce_smem_bytes<kPlain>(S);
     int blocks = 0;
     if (cudaFuncSetAttribute(reduce_kernel<kPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -438,12 +527,10 @@ static int reduce_occupancy(size_t smem)
     return blocks > 0 ? blocks : 1;
 }
 
-// CTAs per SM for either instance (the grid is sized once for both)
-int reduce_ctas_per_sm(uint32_t S)
+// CTAs per SM of the instance with plain BF16 steps (plain) or without
+int reduce_ctas_per_sm(uint32_t S, bool plain)
 {
-    const size_t smem = reduce_smem_bytes(S);
-    const int a = reduce_occupancy<true>(smem), b = reduce_occupancy<false>(smem);
-    return a < b ? a : b;
+    return plain ? reduce_occupancy<true>(S) : reduce_occupancy<false>(S);
 }
 
 }  // namespace zccl
