@@ -47,9 +47,14 @@
  * totals and bases of the device-wide scan (compression also stages each
  * chunk's escapes there, up to 4096 bytes per chunk, so its workspace is
  * about n bytes).  It must be zeroed once before its first use
- * (zccl_workspace_init or any memset to 0); every call leaves it ready for
- * the next one.  A workspace must not be used by two calls that may run at
- * the same time (different streams): they would race.
+ * (zccl_workspace_init or any memset to 0).  A call that ends with
+ * *d_status 0, ZCCL_ERR_CORRUPT_STREAM or ZCCL_ERR_INVALID_ARG leaves it
+ * ready for the next call.  A call that ends with ZCCL_ERR_TIMEOUT (a
+ * device wait ran out, so some CTAs stopped mid-call), or whose launch
+ * failed, may leave its control words mid-call: zero the workspace again
+ * (zccl_workspace_init) before its next use.  A workspace must not be used
+ * by two calls that may run at the same time (different streams): they
+ * would race.
  */
 #ifndef ZCCL_H
 #define ZCCL_H
@@ -227,13 +232,26 @@ zccl_status_t zccl_lut_from_histogram(const uint64_t* hist, zccl_lut_t* lut);
 zccl_status_t zccl_lut_from_data(const uint16_t* d_in, uint64_t n, uint64_t* d_hist, zccl_lut_t* lut,
                                  cudaStream_t stream);
 
-/* Diagnostic of the bounded device waits.  The kernels' only waits are on
- * barriers completed by their own TMA copies; each gives up after a limit
- * and reports ZCCL_ERR_TIMEOUT rather than hang.  This call runs that same
- * wait, with a limit of limit_us microseconds (1..1,000,000), on a barrier
- * that nothing completes, so *d_status must become ZCCL_ERR_TIMEOUT.  The
- * paper has no counterpart; it exists to test the failure path. */
+/* Diagnostics of the bounded device waits.  The kernels wait on two kinds
+ * of things: mbarriers that their own TMA copies complete (every kernel that
+ * stages through shared memory), and -- inside the cooperative compress and
+ * decompress launches -- the call's done counter and the flag words (run
+ * totals, per-chunk entries) that other CTAs of the launch write.  Every
+ * such wait gives up after 1 s and reports ZCCL_ERR_TIMEOUT rather than
+ * hang.  These calls run the same waits, with a limit of limit_us
+ * microseconds (1..1,000,000), on something that never completes, so
+ * *d_status must become ZCCL_ERR_TIMEOUT.  The paper has no counterpart;
+ * they exist to test the failure path.
+ *
+ * zccl_check_bounded_wait: an mbarrier phase nothing completes.
+ * zccl_check_bounded_poll: kind ZCCL_POLL_COUNTER waits, as the done-counter
+ * wait does, for the uint32_t at d_word to reach 1; kind ZCCL_POLL_FLAG
+ * polls, as the flag-word waits do, for bit 63 of the uint64_t at d_word.
+ * d_word: device memory, 8-byte aligned, that the caller keeps at zero. */
 zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cudaStream_t stream);
+enum { ZCCL_POLL_COUNTER = 1, ZCCL_POLL_FLAG = 2 };
+zccl_status_t zccl_check_bounded_poll(int kind, uint32_t limit_us, const void* d_word, uint32_t* d_status,
+                                      cudaStream_t stream);
 
 /* Size of the static device scratch used by zccl_decompress_noalloc, and the
  * largest stream it can decode (the workspace of zccl_decompress for that n
@@ -251,8 +269,10 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
  * library uses a static device array of ZCCL_NOALLOC_SCRATCH_BYTES (1 MiB)
  * that every GPU loading the library holds until the process exits.  n above
  * ZCCL_NOALLOC_MAX_ELEMS returns ZCCL_ERR_INVALID_ARG and queues nothing.
- * The array's device address is looked up on the first call made with a
- * given device current; make that first call before any stream capture.
+ * The array's device address is looked up by the first call made with a
+ * given device current; make that first call before any stream capture.  A
+ * lookup that fails returns ZCCL_ERR_CUDA and is tried again by the next
+ * call.
  * Every call shares the array (the part the call uses is cleared at the
  * start of each call), so calls that overlap on the GPU -- e.g. issued on two
  * streams -- race: serialise them. */

@@ -22,6 +22,7 @@ from . import build as _build
 
 OK, INVALID_ARG, BUFFER_TOO_SMALL, CORRUPT_STREAM, CUDA_ERROR, TIMEOUT = range(6)
 OP_COMPRESS, OP_DECOMPRESS, OP_COMPRESS_BATCHED, OP_DECOMPRESS_REDUCE = range(4)
+POLL_COUNTER, POLL_FLAG = 1, 2
 MAX_SEGMENTS = 4096
 MAX_SHARDS = 1024
 CHUNK = 4096
@@ -63,6 +64,8 @@ _SIGS = {
     "zccl_decompress_noalloc": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
                                  ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "zccl_check_bounded_wait": ([ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "zccl_check_bounded_poll": ([ctypes.c_int, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                                ctypes.c_int),
     "zccl_exponent_histogram": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_void_p], ctypes.c_int),
     "zccl_lut_from_histogram": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
@@ -216,6 +219,10 @@ def zccl_decompress_noalloc(d_in, in_bytes, d_out, n, d_status, stream) -> int:
 
 def zccl_check_bounded_wait(limit_us, d_status, stream) -> int:
     return lib().zccl_check_bounded_wait(limit_us, d_status, stream)
+
+
+def zccl_check_bounded_poll(kind, limit_us, d_word, d_status, stream) -> int:
+    return lib().zccl_check_bounded_poll(kind, limit_us, d_word, d_status, stream)
 
 
 def zccl_rs_plan(ranks, nbytes, ratio, link_gbs, link_latency_us, compress_gbs, compress_fixed_us,

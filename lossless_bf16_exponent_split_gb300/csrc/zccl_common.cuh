@@ -48,6 +48,31 @@ __host__ __device__ inline uint64_t stream_bytes_of(uint64_t n, uint64_t n_esc)
     return zp_offset_of(n) + round_up(n_esc, 128);
 }
 
+// ---- stream header -----------------------------------------------------------
+// The 128-byte header, as 32 little-endian words h[0..31], against the
+// format and the caller's n and in_bytes: magic, version and log2 chunk;
+// n; a LUT of 7 distinct exponents (bytes 24..30) and byte 31 zero;
+// zp_offset equal to its formula; n_esc <= n with the zero-point array
+// inside in_bytes; bytes 40..127 zero.  *n_esc_out = the header's n_esc.
+__device__ __forceinline__ bool header_valid(const uint32_t* h, uint64_t in_bytes, uint64_t n, uint64_t* n_esc_out)
+{
+    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
+    const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
+    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
+    *n_esc_out = n_esc;
+    bool ok = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == n && zp == zp_offset_of(n) &&
+              n_esc <= n && zp + round_up(n_esc, 128) <= in_bytes && (h[7] >> 24) == 0;
+    uint32_t reserved = 0;
+#pragma unroll
+    for (int w = 10; w < 32; ++w) reserved |= h[w];
+    const uint64_t lut = h[6] | ((uint64_t)(h[7] & 0xFFFFFFu) << 32);
+#pragma unroll
+    for (int i = 0; i < 7; ++i)
+#pragma unroll
+        for (int j = i + 1; j < 7; ++j) ok = ok && ((lut >> (8 * i)) & 0xFF) != ((lut >> (8 * j)) & 0xFF);
+    return ok && reserved == 0;
+}
+
 // ---- workspace --------------------------------------------------------------
 // [0, kCtrlBytes): control words, then the flag area (two sets of kMaxGrid
 // 64-bit words, one per call parity); the rest of the workspace is laid out
@@ -174,7 +199,8 @@ __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v)
 // Polls *p until `ready(value)` holds, with back-off; gives up after
 // kSpinTimeoutNs.  Returns the last value read; *ok is false on timeout.
 template <class Ready>
-__device__ __forceinline__ uint64_t poll_u64(const uint64_t* p, Ready ready, bool* ok)
+__device__ __forceinline__ uint64_t poll_u64(const uint64_t* p, Ready ready, bool* ok,
+                                             uint64_t limit_ns = kSpinTimeoutNs)
 {
     uint64_t v = ld_relaxed_u64(p);
     if (ready(v)) return v;
@@ -183,7 +209,7 @@ __device__ __forceinline__ uint64_t poll_u64(const uint64_t* p, Ready ready, boo
         __nanosleep(32);
         v = ld_relaxed_u64(p);
         if (ready(v)) return v;
-        if ((it & 15) == 15 && globaltimer() - t0 > kSpinTimeoutNs) {
+        if ((it & 15) == 15 && globaltimer() - t0 > limit_ns) {
             *ok = false;
             return v;
         }
@@ -477,13 +503,13 @@ __device__ __forceinline__ uint32_t atom_add_release_u32(uint32_t* p, uint32_t v
 
 // Thread 0 only: waits (with back-off, bounded) until *p >= target; false
 // on timeout.  One poller per CTA keeps the polled line from flooding L2.
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target)
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, uint64_t limit_ns = kSpinTimeoutNs)
 {
     uint32_t ns = 64;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
         if (ld_relaxed_u32(p) >= target) return true;
-        if ((it & 7) == 7 && globaltimer() - t0 > kSpinTimeoutNs) return false;
+        if ((it & 7) == 7 && globaltimer() - t0 > limit_ns) return false;
         __nanosleep(ns);
         if (ns < 512) ns <<= 1;
     }

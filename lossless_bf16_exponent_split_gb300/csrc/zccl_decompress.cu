@@ -58,19 +58,14 @@ struct __align__(16) ScanSmem {
     uint32_t last;
 };
 
-// Header checks shared by the scan: magic, version, chunk size, n,
-// zp_offset, and that the zero-point array fits in in_bytes.
+// The scan's header check: a 16-byte aligned stream whose header and blocks
+// fit in in_bytes, and a header that passes header_valid.
 __device__ __forceinline__ bool stream_header_ok(const uint8_t* base, uint64_t in_bytes, uint64_t n,
                                                  uint64_t* n_esc_out)
 {
+    *n_esc_out = 0;
     if (base == nullptr || ((uintptr_t)base & 15) != 0 || in_bytes < zp_offset_of(n)) return false;
-    const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
-    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-    const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-    *n_esc_out = n_esc;
-    return h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == n && zp == zp_offset_of(n) &&
-           n_esc <= n && zp + round_up(n_esc, 128) <= in_bytes;
+    return header_valid(reinterpret_cast<const uint32_t*>(base), in_bytes, n, n_esc_out);
 }
 
 __device__ __forceinline__ const uint8_t* scan_stream(const ScanArgs& a, uint32_t s)
@@ -277,18 +272,6 @@ __device__ __forceinline__ uint32_t run_lo(uint32_t r, uint32_t T, uint32_t G)
     return (uint32_t)(((uint64_t)r * T + G - 1) / G);
 }
 
-// The header checks of stream_header_ok, on a copy of the header.
-__device__ __forceinline__ bool header_words_ok(const uint32_t* h, uint64_t in_bytes, uint64_t n,
-                                                uint64_t* n_esc_out)
-{
-    const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-    const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-    const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-    *n_esc_out = n_esc;
-    return h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == n && zp == zp_offset_of(n) &&
-           n_esc <= n && zp + round_up(n_esc, 128) <= in_bytes;
-}
-
 __device__ __forceinline__ bool entry_ready(uint64_t e) { return (e & kValid) != 0; }
 
 // Thread 0: start the block copy of chunk c into buffer buf (no arrival).
@@ -463,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
     if (tid == 0) {
         bool ok = mbar_wait(&sm.hbar, 0);
         uint64_t n_esc = 0;
-        ok = ok && header_words_ok(sm.hdr, a.in_bytes, a.n, &n_esc);
+        ok = ok && header_valid(sm.hdr, a.in_bytes, a.n, &n_esc);
         sm.hdr_ok = ok && !sm.abort;
         sm.n_esc = n_esc;
         sm.lut_lo = sm.hdr[6] << 8;

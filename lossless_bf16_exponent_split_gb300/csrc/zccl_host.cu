@@ -418,6 +418,17 @@ zccl_status_t zccl_check_bounded_wait(uint32_t limit_us, uint32_t* d_status, cud
     return launch_wait_check((uint64_t)limit_us * 1000, d_status, stream) == cudaSuccess ? ZCCL_OK : ZCCL_ERR_CUDA;
 }
 
+zccl_status_t zccl_check_bounded_poll(int kind, uint32_t limit_us, const void* d_word, uint32_t* d_status,
+                                      cudaStream_t stream)
+{
+    if ((kind != ZCCL_POLL_COUNTER && kind != ZCCL_POLL_FLAG) || d_word == nullptr || !aligned(d_word, 8) ||
+        d_status == nullptr || !aligned(d_status, 4) || limit_us == 0 || limit_us > 1000000)
+        return ZCCL_ERR_INVALID_ARG;
+    return launch_poll_check(kind, (uint64_t)limit_us * 1000, d_word, d_status, stream) == cudaSuccess
+               ? ZCCL_OK
+               : ZCCL_ERR_CUDA;
+}
+
 const char* zccl_status_string(zccl_status_t s)
 {
     switch (s) {

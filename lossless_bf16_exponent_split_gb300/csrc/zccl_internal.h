@@ -133,5 +133,6 @@ cudaError_t launch_histogram(const uint16_t* in, uint64_t n, uint64_t* hist, boo
                              cudaStream_t stream);
 
 cudaError_t launch_wait_check(uint64_t limit_ns, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_poll_check(int kind, uint64_t limit_ns, const void* word, uint32_t* status, cudaStream_t stream);
 
 }  // namespace zccl

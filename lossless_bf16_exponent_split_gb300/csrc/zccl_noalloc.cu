@@ -32,22 +32,24 @@ static_assert(kNoAllocScratchBytes == ZCCL_NOALLOC_SCRATCH_BYTES, "header and li
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-struct ScratchAddress {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
-};
-ScratchAddress g_scratch_address[kMaxDevices];
+std::mutex g_scratch_mutex;
+void* g_scratch_address[kMaxDevices];  // per device; nullptr until a lookup succeeds
 
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current), or nullptr on failure.
+// Device address of the scratch array on the current device, or nullptr on
+// failure.  Looked up with that device current; only a successful lookup is
+// kept, so a failed one (say, a first call made during stream capture) is
+// tried again by the next call.
 void* scratch_on_current_device()
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    ScratchAddress& s = g_scratch_address[dev];
-    std::call_once(s.once, [&]() { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
-    return s.err == cudaSuccess ? s.ptr : nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_address[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        g_scratch_address[dev] = p;
+    }
+    return g_scratch_address[dev];
 }
 
 }  // namespace

@@ -455,11 +455,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const Redu
         bool good = base != nullptr && ((uintptr_t)base & 15) == 0 && in_bytes >= zp_offset_of(a.n);
         if (good) {
             const uint32_t* h = reinterpret_cast<const uint32_t*>(base);
-            const uint64_t hn = h[2] | ((uint64_t)h[3] << 32);
-            const uint64_t n_esc = h[4] | ((uint64_t)h[5] << 32);
-            const uint64_t zp = h[8] | ((uint64_t)h[9] << 32);
-            good = h[0] == kMagic && h[1] == (kVersion | (kLog2Chunk << 16)) && hn == a.n &&
-                   zp == zp_offset_of(a.n) && n_esc <= a.n && zp + round_up(n_esc, 128) <= in_bytes;
+            uint64_t n_esc = 0;
+            good = header_valid(h, in_bytes, a.n, &n_esc);
             t.n_esc[s] = n_esc;
             // LUT bytes, rotated: entry 0 (code 000) unused, entry c = exponent of code c
             t.lut[s] = make_uint2(rot_exp4(h[6] << 8), rot_exp4((h[6] >> 24) | (h[7] << 8)));

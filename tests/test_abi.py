@@ -121,3 +121,12 @@ def test_library_lut_from_histogram_matches_oracle(z, seed):
 def test_library_lut_from_histogram_rejects_bad_size(z):
     with pytest.raises(ValueError):
         z.zccl_lut_from_histogram(np.zeros(255, np.uint64))
+
+
+def test_noalloc_limit_is_the_exact_bound(z):
+    """ZCCL_NOALLOC_MAX_ELEMS (copied into the binding) is the largest n whose
+    decompress workspace fits the 1 MiB static scratch, to the chunk: the
+    workspace of that n fits, one more chunk does not."""
+    assert z.zccl_workspace_bytes(z.OP_DECOMPRESS, z.NOALLOC_MAX_ELEMS) <= z.NOALLOC_SCRATCH_BYTES
+    assert z.zccl_workspace_bytes(z.OP_DECOMPRESS, z.NOALLOC_MAX_ELEMS + 4096) > z.NOALLOC_SCRATCH_BYTES
+    assert z.NOALLOC_MAX_ELEMS % 4096 == 0

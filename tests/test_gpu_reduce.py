@@ -65,6 +65,25 @@ def test_reduce_rejects_wrong_n(codec):
     assert st == 3
 
 
+@pytest.mark.parametrize("off,val", [(25, None), (31, 1), (40, 1), (16, "up")])
+def test_reduce_rejects_corrupt_header(codec, off, val):
+    """A shard whose header breaks the format (a repeated LUT exponent, a
+    nonzero reserved byte, an escape total the planes disagree with) makes
+    the reduction report CORRUPT_STREAM, as the oracle rejects it."""
+    lut = oracle.lut_from_sigma(1.0)
+    n = 2 * 4096 + 300
+    good = [oracle.compress(workloads.gaussian(n, 1.0, seed=s), lut) for s in range(3)]
+    b = bytearray(good[1])
+    b[off] = b[24] if val is None else (b[off] + 1 if val == "up" else val)
+    streams = [good[0], bytes(b), good[2]]
+    assert oracle.decompress_status(streams[1], n)[0] == oracle.CORRUPT
+    st, _ = gpu_reduce(codec, streams, n)
+    assert st == 3
+    # the same workspace-free call path then reduces good shards exactly
+    st, got = gpu_reduce(codec, good, n)
+    assert st == 0 and np.array_equal(got, oracle.decompress_reduce(good, n))
+
+
 def test_rs_local_full(codec):
     cfg = workloads.CONFIGS["rs_local"]
     shards = workloads.reduce_shards(cfg["S"], cfg["n"], cfg["sigma"], seed=0)
