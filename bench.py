@@ -49,11 +49,13 @@ def parse_args():
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="zccl", choices=["zccl", "reference"])
-    p.add_argument("--workload", default="llama3_8b_allgather",
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "rs_local_own",
                             "activation_mix_lut", "gauss1m"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="with the default workload, skip the record of the other workloads")
     return p.parse_args()
 
 
@@ -94,6 +96,10 @@ OP_KERNELS = {"compress": "compress_kernel (one cooperative launch)",
               "decompress_reduce": "escape_scan_kernel + reduce_kernel (PDL pair)",
               "histogram": "hist_zero_kernel + hist_kernel (PDL pair)"}
 OP_LAUNCHES = {"compress": 1, "decompress": 1, "decompress_reduce": 2, "histogram": 2}
+# the headline workload (the 58.7M-element Llama3-8B all-gather payload), and
+# the others that its run also measures and reports under "configs"
+DEFAULT_WORKLOAD = "llama3_8b_allgather"
+CONFIG_WORKLOADS = ["activation_mix", "moe_a2a", "rs_local", "rs_local_own", "activation_mix_lut"]
 # the committed ncu summary of each op's dominant kernel is
 # profiles/<PROFILE_KERNEL[op]>_<workload>.md
 PROFILE_KERNEL = {"compress": "compress_kernel", "decompress": "decompress_kernel",
@@ -261,6 +267,29 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+def config_record(workload: str, m: dict) -> dict:
+    """One workload's entry of the "configs" record: each op's mean time over
+    the back-to-back launches, its algorithmic bytes, achieved GB/s and
+    fraction of the HBM peak, the median single evented launch, the ncu
+    traffic of its dominant kernel (if a summary of the current source is
+    committed), and the clocks seen while it ran."""
+    peak, peak_kind = hbm_peak()
+    ops = {}
+    for nm in m["names"]:
+        ms = m["k_ms"][nm]
+        a = m["alg"][nm] / (ms * 1e-3) / 1e9
+        med = float(np.median(m["single"][nm]))
+        ops[nm] = {"ms": round(ms, 4), "algorithmic_bytes": m["alg"][nm], "achieved_gbs": round(a, 2),
+                   "frac_of_" + peak_kind: round(a / peak, 4),
+                   "single_launch_evented_median_ms": round(med, 4),
+                   "single_launch_frac_of_" + peak_kind: round(m["alg"][nm] / (med * 1e-3) / 1e9 / peak, 4),
+                   "traffic": ncu_traffic(nm, workload)}
+    keep = {k: v for k, v in m["cfg_extra"].items() if k in ("n", "shards", "segments", "stream_bytes",
+                                                             "stream_bytes_total", "ratio", "top7_coverage")}
+    return {"desc": workload_desc(workload), **keep, "ops": ops, "clocks": m["clocks"],
+            "timing": "mean of the back-to-back launches between one event pair, as the headline"}
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -510,315 +539,339 @@ def main():
     build.build()
     z.lib()
 
-    kind, host, sigma, extra = make_inputs(args.workload, seed=rank)
-    lut = z.zccl_lut_from_sigma(sigma)
-    stream = torch.cuda.current_stream()
-    h = int(stream.cuda_stream)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    st_ptr = status.data_ptr()
+    def measure(workload, steps, warmup, with_e2e):
+        """Sets up one workload, times its ops (the timed region, single
+        evented launches, the spread pass) and, if asked and the workload has
+        one, the end-to-end leg; returns what the JSON line reports."""
+        kind, host, sigma, extra = make_inputs(workload, seed=rank)
+        lut = z.zccl_lut_from_sigma(sigma)
+        stream = torch.cuda.current_stream()
+        h = int(stream.cuda_stream)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        st_ptr = status.data_ptr()
 
-    def tdev(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+        def tdev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
 
-    if kind == "roundtrip":
-        n = host.size
-        R = 3
-        xs = [tdev(host) for _ in range(R)]
-        cap = z.zccl_max_compressed_bytes(n)
-        outs = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(R)]
-        nbs = [torch.zeros(1, dtype=torch.int64, device=dev) for _ in range(R)]
-        y = torch.empty(n, dtype=torch.int16, device=dev)
-        wsb = z.zccl_workspace_bytes(z.OP_COMPRESS, n)
-        ws_c = torch.zeros(wsb, dtype=torch.uint8, device=dev)
-        ws_d = torch.zeros(wsb, dtype=torch.uint8, device=dev)
-
-        def comp(r):
-            z.check(z.zccl_compress(xs[r].data_ptr(), n, lut, outs[r].data_ptr(), cap, nbs[r].data_ptr(),
-                                    ws_c.data_ptr(), wsb, st_ptr, h), "compress")
-
-        def decomp(r):
-            z.check(z.zccl_decompress(outs[r].data_ptr(), cap, y.data_ptr(), n, ws_d.data_ptr(), wsb, st_ptr, h),
-                    "decompress")
-
-        for r in range(R):
-            comp(r)
-        torch.cuda.synchronize()
-        stream_bytes = int(nbs[0].item())
-        names = ["compress", "decompress"]
-        alg = {"compress": 2 * n + stream_bytes, "decompress": stream_bytes + 2 * n}
-        step_input_bytes = 2 * 2 * n
-
-        # decompress reads a stream compressed one launch before or after in
-        # the rotation, never the one just written (part of it is still in L2):
-        # not in the interleaved single-launch timing, nor at the start of the
-        # decompress batch, which follows the whole compress batch
-        off = decompress_offset(args.warmup, args.steps, R)
-        ops = [("compress", lambda k: comp(k % R)), ("decompress", lambda k: decomp((k + off) % R))]
-        cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
-                     "step": "compress batch k + decompress the stream of batch k-1 (k+1 in the rotation "
-                             "when k-1's buffer is the one the compress batch wrote last)",
-                     "l2": "3 rotating buffer sets, >316 MB touched per step (> 129 MB L2)"}
-    elif kind == "batched":
-        m = extra
-        payload = tdev(host)
-        segs = []
-        hid = m.hidden
-        outs = []
-        for (r0, rows) in m.segments:
-            nn = rows * hid
-            cap = z.zccl_max_compressed_bytes(nn)
-            o = torch.empty(cap, dtype=torch.uint8, device=dev)
-            outs.append(o)
-            segs.append((payload[r0 * hid:(r0 + rows) * hid], o))
-        codec = z.Codec(dev)
-        table = codec.segment_table(segs)
-        total_n = host.size
-        nb = torch.zeros(len(segs), dtype=torch.int64, device=dev)
-        wsb = z.zccl_workspace_bytes(z.OP_COMPRESS_BATCHED, total_n, len(segs))
-        ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
-
-        def comp():
-            z.check(z.zccl_compress_batched(table.data_ptr(), len(segs), total_n, lut, nb.data_ptr(),
-                                            ws.data_ptr(), wsb, st_ptr, h), "compress_batched")
-        comp()
-        torch.cuda.synchronize()
-        sb = int(nb.sum().item())
-        names = ["compress"]
-        alg = {"compress": 2 * total_n + sb}
-        step_input_bytes = 2 * total_n
-
-        ops = [("compress", lambda k: comp())]
-        cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
-                     "step": "one batched compress of all static+dynamic segments",
-                     "l2": "input 537 MB > 129 MB L2"}
-    elif kind == "histogram":
-        n = host.size
-        R = 5
-        xs = [tdev(host) for _ in range(R)]
-        hist = torch.empty(256, dtype=torch.int64, device=dev)
-
-        def hist_call(r):
-            z.check(z.zccl_exponent_histogram(xs[r].data_ptr(), n, hist.data_ptr(), 0, h), "exponent_histogram")
-        names = ["histogram"]
-        alg = {"histogram": 2 * n + 256 * 8}
-        step_input_bytes = 2 * n
-
-        ops = [("histogram", lambda k: hist_call(k % R))]
-        hist_call(0)
-        hh0 = hist.cpu().numpy().view(np.uint64).astype(np.float64)
-        lut_data = z.zccl_lut_from_histogram(hist.cpu().numpy().view(np.uint64))
-        coverage = {"sigma_lut": round(float(hh0[list(lut)].sum() / n), 6),
-                    "data_lut": round(float(hh0[list(lut_data)].sum() / n), 6),
-                    "sigma": sigma, "data_lut_exponents": list(lut_data)}
-        cfg_extra = {"n": n, "step": "one exponent histogram pass (zeroing + counting kernel, PDL pair)",
-                     "top7_coverage": coverage,
-                     "l2": f"5 rotating inputs; {4 * 2 * n >> 20} MiB read between two reads of one (> 129 MB L2)"}
-    else:  # reduce (with the rank's own shard uncompressed at local_pos, if given)
-        shards = host
-        local_pos = extra
-        S = len(shards)
-        n = shards[0].size
-        codec = z.Codec(dev)
-        # three copies of the step's inputs (streams, local shard) and outputs,
-        # used in rotation: two other calls (442 MB) run between two reads of one
-        R = 3
-        sets = []
-        for _ in range(R):
-            streams, sizes = [], []
-            for s_, x in enumerate(shards):
-                if s_ == local_pos:
-                    streams.append(None)
-                    sizes.append(None)
-                    continue
-                o, nbt = codec.compress(tdev(x), lut)
-                streams.append(o)
-                sizes.append(nbt)
-            torch.cuda.synchronize()
-            sizes_h = [0 if v is None else int(v.item()) for v in sizes]
-            ptrs = torch.tensor([0 if o is None else o.data_ptr() for o in streams], dtype=torch.int64, device=dev)
-            inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
-            local = tdev(shards[local_pos]) if local_pos is not None else None
+        if kind == "roundtrip":
+            n = host.size
+            R = 3
+            xs = [tdev(host) for _ in range(R)]
+            cap = z.zccl_max_compressed_bytes(n)
+            outs = [torch.empty(cap, dtype=torch.uint8, device=dev) for _ in range(R)]
+            nbs = [torch.zeros(1, dtype=torch.int64, device=dev) for _ in range(R)]
             y = torch.empty(n, dtype=torch.int16, device=dev)
-            sets.append((streams, ptrs, inb, local, y))
-        wsb = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, n, S)
-        ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+            wsb = z.zccl_workspace_bytes(z.OP_COMPRESS, n)
+            ws_c = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+            ws_d = torch.zeros(wsb, dtype=torch.uint8, device=dev)
 
-        def red(k):
-            _, ptrs, inb, local, y = sets[k % R]
-            if local is None:
-                z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n,
-                                                 ws.data_ptr(), wsb, st_ptr, h), "decompress_reduce")
-            else:
-                z.check(z.zccl_decompress_reduce_local(ptrs.data_ptr(), inb.data_ptr(), S, local.data_ptr(),
-                                                       local_pos, 0, y.data_ptr(), n, ws.data_ptr(), wsb, st_ptr,
-                                                       h), "decompress_reduce_local")
-        names = ["decompress_reduce"]
-        alg = {"decompress_reduce": sum(sizes_h) + (2 * n if local_pos is not None else 0) + 2 * n}
-        step_input_bytes = 2 * S * n
-        ops = [("decompress_reduce", red)]
-        cfg_extra = {"n": n, "shards": S, "stream_bytes_total": sum(sizes_h),
-                     "step": "one fused decompress+reduce of S shards"
-                             + (f" (shard {local_pos} uncompressed)" if local_pos is not None else ""),
-                     "l2": f"{R} rotating copies of the inputs and output; "
-                           f"{(R - 1) * (sum(sizes_h) + 2 * n + (2 * n if local_pos is not None else 0)) >> 20} MiB "
-                           "touched between two reads of one (> 129 MB L2)"}
+            def comp(r):
+                z.check(z.zccl_compress(xs[r].data_ptr(), n, lut, outs[r].data_ptr(), cap, nbs[r].data_ptr(),
+                                        ws_c.data_ptr(), wsb, st_ptr, h), "compress")
 
-    # ---- warm-up, then K timed steps ----
-    for k in range(args.warmup):
-        for _, fn in ops:
-            fn(k + 1)
-    torch.cuda.synchronize()
-    status.zero_()
-    op_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    barrier(pg, dev)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        # a ~1 ms GPU sleep before the start event gives the host a head start,
-        # so no event brackets time the GPU spends waiting for the host to
-        # enqueue (the sleep itself is outside the timed region)
-        torch.cuda._sleep(2_000_000)
-        t_start.record(stream)
-        # the K steps' work op by op: each op's K launches run back to back
-        # between one pair of events, so a launch's time is its share of that
-        # span (an event pair around every launch would also time the event's
-        # wait for the previous kernel to drain)
-        for (nm, fn), (e0, e1) in zip(ops, op_ev):
-            e0.record(stream)
-            for k in range(args.steps):
-                fn(args.warmup + 1 + k)
-            e1.record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-    barrier(pg, dev)
-    st = int(status.item())
-    if st != 0:
-        raise SystemExit(f"device status {st} ({z.status_string(st)}) during the timed region")
-    k_ms = {nm: e0.elapsed_time(e1) / args.steps for (nm, _), (e0, e1) in zip(ops, op_ev)}
-    region_ms = t_start.elapsed_time(t_end)
-    ms_per_step = max_over_ranks(pg, region_ms / args.steps, dev)
-    value = aggregate_gbs(world, step_input_bytes, ms_per_step)
+            def decomp(r):
+                z.check(z.zccl_decompress(outs[r].data_ptr(), cap, y.data_ptr(), n, ws_d.data_ptr(), wsb, st_ptr, h),
+                        "decompress")
 
-    # ---- the same launches one at a time, each between its own events ----
-    # (outside the timed region: what a caller timing a single call sees)
-    S1 = min(args.steps, 10)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(S1)]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(2_000_000)
-    for k in range(S1):
-        sev[k][0].record(stream)
-        for i, (_, fn) in enumerate(ops):
-            fn(args.warmup + args.steps + 1 + k)
-            sev[k][i + 1].record(stream)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise SystemExit(f"device status {int(status.item())} after the single-launch timing")
-    single = {nm: [sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(S1)] for i, (nm, _) in enumerate(ops)}
+            for r in range(R):
+                comp(r)
+            torch.cuda.synchronize()
+            stream_bytes = int(nbs[0].item())
+            names = ["compress", "decompress"]
+            alg = {"compress": 2 * n + stream_bytes, "decompress": stream_bytes + 2 * n}
+            step_input_bytes = 2 * 2 * n
 
-    # ---- spread: the same back-to-back runs again, with events at the
-    # boundaries of up to 6 groups (each inner event adds a drain, so these
-    # group means are a little above the timed region's) ----
-    bounds = group_bounds(args.steps)
-    n_groups = len(bounds) - 1
-    gev = [[torch.cuda.Event(enable_timing=True) for _ in bounds] for _ in ops]
-    torch.cuda.synchronize()
-    torch.cuda._sleep(2_000_000)
-    for (nm, fn), evs in zip(ops, gev):
-        evs[0].record(stream)
-        for g in range(n_groups):
-            for k in range(bounds[g], bounds[g + 1]):
-                fn(args.warmup + args.steps + S1 + 1 + k)
-            evs[g + 1].record(stream)
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise SystemExit(f"device status {int(status.item())} after the spread pass")
-    k_groups = {nm: [evs[g].elapsed_time(evs[g + 1]) / (bounds[g + 1] - bounds[g]) for g in range(n_groups)]
-                for (nm, _), evs in zip(ops, gev)}
+            # decompress reads a stream compressed one launch before or after in
+            # the rotation, never the one just written (part of it is still in L2):
+            # not in the interleaved single-launch timing, nor at the start of the
+            # decompress batch, which follows the whole compress batch
+            off = decompress_offset(warmup, steps, R)
+            ops = [("compress", lambda k: comp(k % R)), ("decompress", lambda k: decomp((k + off) % R))]
+            cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
+                         "step": "compress batch k + decompress the stream of batch k-1 (k+1 in the rotation "
+                                 "when k-1's buffer is the one the compress batch wrote last)",
+                         "l2": "3 rotating buffer sets, >316 MB touched per step (> 129 MB L2)"}
+        elif kind == "batched":
+            m = extra
+            payload = tdev(host)
+            segs = []
+            hid = m.hidden
+            outs = []
+            for (r0, rows) in m.segments:
+                nn = rows * hid
+                cap = z.zccl_max_compressed_bytes(nn)
+                o = torch.empty(cap, dtype=torch.uint8, device=dev)
+                outs.append(o)
+                segs.append((payload[r0 * hid:(r0 + rows) * hid], o))
+            codec = z.Codec(dev)
+            table = codec.segment_table(segs)
+            total_n = host.size
+            nb = torch.zeros(len(segs), dtype=torch.int64, device=dev)
+            wsb = z.zccl_workspace_bytes(z.OP_COMPRESS_BATCHED, total_n, len(segs))
+            ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
 
-    # ---- end to end through the C ABI with host buffers ----
-    e2e = None
-    if kind == "roundtrip" and not args.no_e2e:
-        # Pipelined as a user would: step k's upload (pinned host -> device)
-        # runs on one copy stream and step k-1's download on another while
-        # step k-1's compress + decompress run, with two buffer slots.  Every
-        # step's copies are inside the timed region.
-        hx = torch.from_numpy(host.view(np.int16)).pin_memory()
-        hy = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-        hnb = [torch.empty(1, dtype=torch.int64).pin_memory() for _ in range(2)]
-        ys = [y, torch.empty(n, dtype=torch.int16, device=dev)]
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        in_done = [torch.cuda.Event() for _ in range(2)]
-        comp_done = [torch.cuda.Event() for _ in range(2)]
-        out_done = [torch.cuda.Event() for _ in range(2)]
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
+            def comp():
+                z.check(z.zccl_compress_batched(table.data_ptr(), len(segs), total_n, lut, nb.data_ptr(),
+                                                ws.data_ptr(), wsb, st_ptr, h), "compress_batched")
+            comp()
+            torch.cuda.synchronize()
+            sb = int(nb.sum().item())
+            names = ["compress"]
+            alg = {"compress": 2 * total_n + sb}
+            step_input_bytes = 2 * total_n
 
-        def e2e_step(k):
-            i = k % 2
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(comp_done[i])  # step k-2 has finished reading slot i
-                xs[i].copy_(hx, non_blocking=True)
-                in_done[i].record(s_in)
-            stream.wait_event(in_done[i])
-            stream.wait_event(out_done[i])  # step k-2's download has read ys[i]
-            comp(i)
-            z.check(z.zccl_decompress(outs[i].data_ptr(), cap, ys[i].data_ptr(), n, ws_d.data_ptr(), wsb, st_ptr,
-                                      h), "decompress")
-            comp_done[i].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(comp_done[i])
-                hy[i].copy_(ys[i], non_blocking=True)
-                hnb[i].copy_(nbs[i], non_blocking=True)
-                out_done[i].record(s_out)
-        for k in range(2):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        s_in.wait_event(ev0)
-        s_out.wait_event(ev0)
-        for k in range(args.steps):
-            e2e_step(k)
-        stream.wait_event(out_done[0])
-        stream.wait_event(out_done[1])
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = ev0.elapsed_time(ev1) / args.steps
-        e2e_ms = max_over_ranks(pg, e2e_ms, dev)
-        for i in range(min(2, args.steps)):
-            assert np.array_equal(hy[i].numpy().view(np.uint16), host), "e2e round trip not bit-exact"
-        e2e = {"value": round(world * 2 * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 8,
-               "path": "pinned host -> H2D -> zccl_compress -> zccl_decompress -> D2H, "
-                       "uploads and downloads of neighbouring steps overlapped on two copy streams"}
+            ops = [("compress", lambda k: comp())]
+            cfg_extra = {"n": total_n, "segments": len(segs), "stream_bytes": sb,
+                         "step": "one batched compress of all static+dynamic segments",
+                         "l2": "input 537 MB > 129 MB L2"}
+        elif kind == "histogram":
+            n = host.size
+            R = 5
+            xs = [tdev(host) for _ in range(R)]
+            hist = torch.empty(256, dtype=torch.int64, device=dev)
 
-    if kind == "histogram" and not args.no_e2e:
-        hx = torch.from_numpy(host.view(np.int16)).pin_memory()
-        hh = torch.empty(256, dtype=torch.int64).pin_memory()
-        luts = []
+            def hist_call(r):
+                z.check(z.zccl_exponent_histogram(xs[r].data_ptr(), n, hist.data_ptr(), 0, h), "exponent_histogram")
+            names = ["histogram"]
+            alg = {"histogram": 2 * n + 256 * 8}
+            step_input_bytes = 2 * n
 
-        def e2e_step():
-            xs[0].copy_(hx, non_blocking=True)
+            ops = [("histogram", lambda k: hist_call(k % R))]
             hist_call(0)
-            hh.copy_(hist, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-            luts.append(z.zccl_lut_from_histogram(hh.numpy().view(np.uint64)))
-        for _ in range(2):
-            e2e_step()
+            hh0 = hist.cpu().numpy().view(np.uint64).astype(np.float64)
+            lut_data = z.zccl_lut_from_histogram(hist.cpu().numpy().view(np.uint64))
+            coverage = {"sigma_lut": round(float(hh0[list(lut)].sum() / n), 6),
+                        "data_lut": round(float(hh0[list(lut_data)].sum() / n), 6),
+                        "sigma": sigma, "data_lut_exponents": list(lut_data)}
+            cfg_extra = {"n": n, "step": "one exponent histogram pass (zeroing + counting kernel, PDL pair)",
+                         "top7_coverage": coverage,
+                         "l2": f"5 rotating inputs; {4 * 2 * n >> 20} MiB read between two reads of one (> 129 MB L2)"}
+        else:  # reduce (with the rank's own shard uncompressed at local_pos, if given)
+            shards = host
+            local_pos = extra
+            S = len(shards)
+            n = shards[0].size
+            codec = z.Codec(dev)
+            # three copies of the step's inputs (streams, local shard) and outputs,
+            # used in rotation: two other calls (442 MB) run between two reads of one
+            R = 3
+            sets = []
+            for _ in range(R):
+                streams, sizes = [], []
+                for s_, x in enumerate(shards):
+                    if s_ == local_pos:
+                        streams.append(None)
+                        sizes.append(None)
+                        continue
+                    o, nbt = codec.compress(tdev(x), lut)
+                    streams.append(o)
+                    sizes.append(nbt)
+                torch.cuda.synchronize()
+                sizes_h = [0 if v is None else int(v.item()) for v in sizes]
+                ptrs = torch.tensor([0 if o is None else o.data_ptr() for o in streams], dtype=torch.int64, device=dev)
+                inb = torch.tensor(sizes_h, dtype=torch.int64, device=dev)
+                local_x = tdev(shards[local_pos]) if local_pos is not None else None
+                y = torch.empty(n, dtype=torch.int16, device=dev)
+                sets.append((streams, ptrs, inb, local_x, y))
+            wsb = z.zccl_workspace_bytes(z.OP_DECOMPRESS_REDUCE, n, S)
+            ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+
+            def red(k):
+                _, ptrs, inb, local_x, y = sets[k % R]
+                if local_x is None:
+                    z.check(z.zccl_decompress_reduce(ptrs.data_ptr(), inb.data_ptr(), S, y.data_ptr(), n,
+                                                     ws.data_ptr(), wsb, st_ptr, h), "decompress_reduce")
+                else:
+                    z.check(z.zccl_decompress_reduce_local(ptrs.data_ptr(), inb.data_ptr(), S, local_x.data_ptr(),
+                                                           local_pos, 0, y.data_ptr(), n, ws.data_ptr(), wsb, st_ptr,
+                                                           h), "decompress_reduce_local")
+            names = ["decompress_reduce"]
+            alg = {"decompress_reduce": sum(sizes_h) + (2 * n if local_pos is not None else 0) + 2 * n}
+            step_input_bytes = 2 * S * n
+            ops = [("decompress_reduce", red)]
+            cfg_extra = {"n": n, "shards": S, "stream_bytes_total": sum(sizes_h),
+                         "step": "one fused decompress+reduce of S shards"
+                                 + (f" (shard {local_pos} uncompressed)" if local_pos is not None else ""),
+                         "l2": f"{R} rotating copies of the inputs and output; "
+                               f"{(R - 1) * (sum(sizes_h) + 2 * n + (2 * n if local_pos is not None else 0)) >> 20} MiB "
+                               "touched between two reads of one (> 129 MB L2)"}
+
+        # ---- warm-up, then K timed steps ----
+        for k in range(warmup):
+            for _, fn in ops:
+                fn(k + 1)
         torch.cuda.synchronize()
+        status.zero_()
+        op_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
         barrier(pg, dev)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-        e2e_ms = max_over_ranks(pg, e2e_ms, dev)
-        assert len(set(luts)) == 1
-        e2e = {"value": round(world * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 256 * 8,
-               "path": "pinned host -> H2D -> zccl_exponent_histogram -> D2H -> zccl_lut_from_histogram",
-               "lut": list(luts[0])}
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            wall0 = time.perf_counter()
+            # a ~1 ms GPU sleep before the start event gives the host a head start,
+            # so no event brackets time the GPU spends waiting for the host to
+            # enqueue (the sleep itself is outside the timed region)
+            torch.cuda._sleep(2_000_000)
+            t_start.record(stream)
+            # the K steps' work op by op: each op's K launches run back to back
+            # between one pair of events, so a launch's time is its share of that
+            # span (an event pair around every launch would also time the event's
+            # wait for the previous kernel to drain)
+            for (nm, fn), (e0, e1) in zip(ops, op_ev):
+                e0.record(stream)
+                for k in range(steps):
+                    fn(warmup + 1 + k)
+                e1.record(stream)
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - wall0
+        barrier(pg, dev)
+        st = int(status.item())
+        if st != 0:
+            raise SystemExit(f"device status {st} ({z.status_string(st)}) during the timed region")
+        k_ms = {nm: e0.elapsed_time(e1) / steps for (nm, _), (e0, e1) in zip(ops, op_ev)}
+        region_ms = t_start.elapsed_time(t_end)
+        ms_per_step = max_over_ranks(pg, region_ms / steps, dev)
+        value = aggregate_gbs(world, step_input_bytes, ms_per_step)
+
+        # ---- the same launches one at a time, each between its own events ----
+        # (outside the timed region: what a caller timing a single call sees)
+        S1 = min(steps, 10)
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(S1)]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(2_000_000)
+        for k in range(S1):
+            sev[k][0].record(stream)
+            for i, (_, fn) in enumerate(ops):
+                fn(warmup + steps + 1 + k)
+                sev[k][i + 1].record(stream)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise SystemExit(f"device status {int(status.item())} after the single-launch timing")
+        single = {nm: [sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(S1)] for i, (nm, _) in enumerate(ops)}
+
+        # ---- spread: the same back-to-back runs again, with events at the
+        # boundaries of up to 6 groups (each inner event adds a drain, so these
+        # group means are a little above the timed region's) ----
+        bounds = group_bounds(steps)
+        n_groups = len(bounds) - 1
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in bounds] for _ in ops]
+        torch.cuda.synchronize()
+        torch.cuda._sleep(2_000_000)
+        for (nm, fn), evs in zip(ops, gev):
+            evs[0].record(stream)
+            for g in range(n_groups):
+                for k in range(bounds[g], bounds[g + 1]):
+                    fn(warmup + steps + S1 + 1 + k)
+                evs[g + 1].record(stream)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise SystemExit(f"device status {int(status.item())} after the spread pass")
+        k_groups = {nm: [evs[g].elapsed_time(evs[g + 1]) / (bounds[g + 1] - bounds[g]) for g in range(n_groups)]
+                    for (nm, _), evs in zip(ops, gev)}
+
+        # ---- end to end through the C ABI with host buffers ----
+        e2e = None
+        if kind == "roundtrip" and not (not with_e2e):
+            # Pipelined as a user would: step k's upload (pinned host -> device)
+            # runs on one copy stream and step k-1's download on another while
+            # step k-1's compress + decompress run, with two buffer slots.  Every
+            # step's copies are inside the timed region.
+            hx = torch.from_numpy(host.view(np.int16)).pin_memory()
+            hy = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
+            hnb = [torch.empty(1, dtype=torch.int64).pin_memory() for _ in range(2)]
+            ys = [y, torch.empty(n, dtype=torch.int16, device=dev)]
+            s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+            in_done = [torch.cuda.Event() for _ in range(2)]
+            comp_done = [torch.cuda.Event() for _ in range(2)]
+            out_done = [torch.cuda.Event() for _ in range(2)]
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+
+            def e2e_step(k):
+                i = k % 2
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(comp_done[i])  # step k-2 has finished reading slot i
+                    xs[i].copy_(hx, non_blocking=True)
+                    in_done[i].record(s_in)
+                stream.wait_event(in_done[i])
+                stream.wait_event(out_done[i])  # step k-2's download has read ys[i]
+                comp(i)
+                z.check(z.zccl_decompress(outs[i].data_ptr(), cap, ys[i].data_ptr(), n, ws_d.data_ptr(), wsb, st_ptr,
+                                          h), "decompress")
+                comp_done[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_done[i])
+                    hy[i].copy_(ys[i], non_blocking=True)
+                    hnb[i].copy_(nbs[i], non_blocking=True)
+                    out_done[i].record(s_out)
+            for k in range(2):
+                e2e_step(k)
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            s_in.wait_event(ev0)
+            s_out.wait_event(ev0)
+            for k in range(steps):
+                e2e_step(k)
+            stream.wait_event(out_done[0])
+            stream.wait_event(out_done[1])
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms = ev0.elapsed_time(ev1) / steps
+            e2e_ms = max_over_ranks(pg, e2e_ms, dev)
+            for i in range(min(2, steps)):
+                assert np.array_equal(hy[i].numpy().view(np.uint16), host), "e2e round trip not bit-exact"
+            e2e = {"value": round(world * 2 * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                   "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n + 8,
+                   "path": "pinned host -> H2D -> zccl_compress -> zccl_decompress -> D2H, "
+                           "uploads and downloads of neighbouring steps overlapped on two copy streams"}
+
+        if kind == "histogram" and not (not with_e2e):
+            hx = torch.from_numpy(host.view(np.int16)).pin_memory()
+            hh = torch.empty(256, dtype=torch.int64).pin_memory()
+            luts = []
+
+            def e2e_step():
+                xs[0].copy_(hx, non_blocking=True)
+                hist_call(0)
+                hh.copy_(hist, non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+                luts.append(z.zccl_lut_from_histogram(hh.numpy().view(np.uint64)))
+            for _ in range(2):
+                e2e_step()
+            torch.cuda.synchronize()
+            barrier(pg, dev)
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                e2e_step()
+            e2e_ms = (time.perf_counter() - t0) * 1e3 / steps
+            e2e_ms = max_over_ranks(pg, e2e_ms, dev)
+            assert len(set(luts)) == 1
+            e2e = {"value": round(world * 2 * n / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                   "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 256 * 8,
+                   "path": "pinned host -> H2D -> zccl_exponent_histogram -> D2H -> zccl_lut_from_histogram",
+                   "lut": list(luts[0])}
+
+        return {"kind": kind, "names": names, "alg": alg, "k_ms": k_ms, "single": single, "k_groups": k_groups,
+                "clocks": clk.summary(), "wall": wall, "ms_per_step": ms_per_step, "value": value,
+                "cfg_extra": cfg_extra, "e2e": e2e, "step_input_bytes": step_input_bytes}
+
+    m = measure(args.workload, args.steps, args.warmup, not args.no_e2e)
+    names, alg, k_ms, single, k_groups = m["names"], m["alg"], m["k_ms"], m["single"], m["k_groups"]
+    ms_per_step, value, cfg_extra, e2e, wall = m["ms_per_step"], m["value"], m["cfg_extra"], m["e2e"], m["wall"]
+    step_input_bytes = m["step_input_bytes"]
+    # every other workload, measured the same way (fewer steps) and reported
+    # beside the headline, when the default workload runs on one GPU
+    configs = None
+    if args.workload == DEFAULT_WORKLOAD and world == 1 and not args.no_configs:
+        configs = {}
+        for w in CONFIG_WORKLOADS:
+            mm = measure(w, min(args.steps, 20), min(args.warmup, 3), False)
+            configs[w] = config_record(w, mm)
+            del mm
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -857,11 +910,13 @@ def main():
                      "algorithmic_bytes_per_launch": alg[dom]},
         "kernels": kernels,
         "gpu_launches": sum(OP_LAUNCHES[nm] for nm in names) * args.steps,
-        "clocks": clk.summary(),
+        "clocks": m["clocks"],
         "wall_s_timed_region": round(wall, 4),
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if configs is not None:
+        line["configs"] = configs
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.workload)
