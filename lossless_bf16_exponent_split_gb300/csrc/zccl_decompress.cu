@@ -151,10 +151,14 @@ __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs
 
     for (uint32_t r = blockIdx.x; r < nr; r += gridDim.x) {
         const uint32_t s = r / rps, q = r % rps;
+        // Counting needs only that the stream's blocks are there; the header
+        // itself is checked once, by the CTA that scans the range totals (and
+        // again by the reduce kernel before it uses it).  (The plain BF16
+        // position, if any, has no stream: zero counts.)
         if (tid == 0) {
-            uint64_t n_esc;
-            // (the plain BF16 position, if any, has no stream: zero counts)
-            sm.hdr_ok = s != a.skip && stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc);
+            const uint8_t* base = scan_stream(a, s);
+            sm.hdr_ok = s != a.skip && base != nullptr && ((uintptr_t)base & 15) == 0 &&
+                        scan_in_bytes(a, s) >= zp_offset_of(a.n);
         }
         __syncthreads();
         const uint32_t c0 = q * kRangeChunks;
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs
     }
     pdl_launch_dependents();
     if (arrive_last(a.ctrl, &sm.last)) {
-        cta_segmented_exclusive_scan<kThreads, 4>(
+        cta_segmented_exclusive_scan<kThreads, 8>(
             a.totals, a.bases, nr, [&](uint32_t r) { return r % rps == 0; }, sm.scan64, sm.scan_f);
         __syncthreads();
         // every stream's recount must equal its header's escape count
