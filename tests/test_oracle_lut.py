@@ -48,9 +48,9 @@ def test_lut_matches_high_precision_ranking(sigma, expect_cov):
 
 
 def test_lut_sigma_sweep():
-    """sigma = 2^f, f in [-20, 10] step 1/16: oracle ranks == 40-digit ranks."""
-    for i in range(0, 30 * 16 + 1):
-        sigma = 2.0 ** (-20 + i / 16)
+    """sigma = 2^f, f in [-20, 10] step 1/64: oracle ranks == 40-digit ranks."""
+    for i in range(0, 30 * 64 + 1):
+        sigma = 2.0 ** (-20 + i / 64)
         top, _ = mp_top7(sigma)
         assert list(oracle.lut_from_sigma(sigma)) == top, sigma
 
