@@ -44,7 +44,7 @@
  *
  * Workspace: a device buffer of zccl_workspace_bytes() bytes that holds a
  * call's intermediate results: per-chunk escape counts and the per-range
- * totals and bases of the device-wide scan (compression also stages each
+ * look-back words and bases of the device-wide scan (compression also stages each
  * chunk's escapes there, up to 4096 bytes per chunk, so its workspace is
  * about n bytes).  It must be zeroed once before its first use
  * (zccl_workspace_init or any memset to 0).  A call that ends with
@@ -235,8 +235,9 @@ zccl_status_t zccl_lut_from_data(const uint16_t* d_in, uint64_t n, uint64_t* d_h
 /* Diagnostics of the bounded device waits.  The kernels wait on two kinds
  * of things: mbarriers that their own TMA copies complete (every kernel that
  * stages through shared memory), and -- inside the cooperative compress and
- * decompress launches -- the call's done counter and the flag words (run
- * totals, per-chunk entries) that other CTAs of the launch write.  Every
+ * decompress launches and the escape scan of decompress-reduce -- the
+ * call's done counter and the flag words (run totals, per-chunk entries,
+ * per-range look-back words) that other CTAs of the launch write.  Every
  * such wait gives up after 1 s and reports ZCCL_ERR_TIMEOUT rather than
  * hang.  These calls run the same waits, with a limit of limit_us
  * microseconds (1..1,000,000), on something that never completes, so

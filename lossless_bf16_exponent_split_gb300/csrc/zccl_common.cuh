@@ -102,6 +102,8 @@ struct WsCtrl {
     uint32_t pad5[30];
     uint32_t done[2];       // progress count of the running call, by call parity
     uint32_t pad4[30];
+    unsigned long long sticket;  // escape scan: range tickets of the running call
+    uint32_t pad6[30];
     uint32_t top;           // arrivals of the group leaders (own 32-byte sector)
     uint32_t pad3[7];
     struct {
@@ -118,9 +120,17 @@ constexpr uint64_t kPrefixBytes = kCtrlBytes + kFlagBytes;
 // A published 64-bit flag word: bit 63 set, the value in the low bits.
 constexpr uint64_t kValid = 1ull << 63;
 
-// Chunks per range: the unit of the per-range escape totals that one CTA
-// scans at the end of a pass.
+// Chunks per range: the unit of the escape scan's per-range totals.
 constexpr uint32_t kRangeChunks = 32;
+
+// Look-back word of one range of the escape scan: the state in bits 62..63
+// (0: not yet published; kLbAggregate: the value is the range's own escape
+// total; kLbInclusive: the value is the escapes of its stream up to and
+// including the range) and the value in bits 0..61.
+constexpr uint64_t kLbState = 3ull << 62;
+constexpr uint64_t kLbAggregate = 1ull << 62;
+constexpr uint64_t kLbInclusive = 2ull << 62;
+constexpr uint64_t kLbValue = (1ull << 62) - 1;
 
 // A chunk's quarter word, written by the escape scan for the fused
 // reduction: the escapes before quarter q (q = 1, 2, 3; a quarter is 1024
@@ -561,33 +571,6 @@ __device__ __forceinline__ int64_t block_max_i64(int64_t v, int64_t* scratch)
     return t;
 }
 
-// ---- exclusive scan by one CTA -----------------------------------------------------
-// out[r] = in[0] + ... + in[r-1] for r < R (R <= kThreads * K per tile; larger
-// R runs tile by tile).  Loads bypass L1 (the inputs were written by other
-// CTAs); each thread's K loads are all in flight at once.  Contains barriers.
-template <int kThreads, int K>
-__device__ void cta_exclusive_scan(const uint32_t* in, uint64_t* out, uint32_t R, uint64_t* scratch)
-{
-    uint64_t carry = 0;
-    for (uint32_t base = 0; base < R; base += kThreads * K) {
-        const uint32_t first = base + threadIdx.x * K;
-        uint32_t v[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) v[j] = first + j < R ? __ldcg(in + first + j) : 0u;
-        uint64_t mine = 0;
-#pragma unroll
-        for (int j = 0; j < K; ++j) mine += v[j];
-        uint64_t tile;
-        uint64_t run = carry + block_exclusive_scan<kThreads, uint64_t>(mine, scratch, &tile);
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (first + j < R) out[first + j] = run;
-            run += v[j];
-        }
-        carry += tile;
-    }
-}
-
 // ---- segmented exclusive scan of one value per thread -------------------------
 // Thread t holds (head_t, v_t) in order t = 0..kThreads-1, after a carry-in
 // state `carry` (the sum since the last segment start before thread 0).
@@ -629,86 +612,6 @@ __device__ __forceinline__ uint64_t seg_block_excl_scan(bool head, uint64_t v, u
     __syncthreads();
     *carry_out = tx;
     return head ? 0 : px;
-}
-
-// ---- segmented exclusive scan by one CTA --------------------------------------
-// out[r] = sum of in[q] for q in [head(r), r), where head(r) is the first
-// index of r's segment (is_head(q) marks segment starts).  One CTA of
-// kThreads threads, K values per thread per tile; loads bypass L1 (the
-// inputs were written by other CTAs).  Contains barriers.
-template <int kThreads, int K, class IsHead>
-__device__ void cta_segmented_exclusive_scan(const uint32_t* in, uint64_t* out, uint32_t R, IsHead is_head,
-                                             uint64_t* sv /*[kThreads/32]*/, uint32_t* sf /*[kThreads/32]*/)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint64_t carry_v = 0;  // state after the previous tile
-    for (uint32_t base = 0; base < R; base += kThreads * K) {
-        const uint32_t first = base + threadIdx.x * K;
-        uint64_t v[K], loc[K];
-        bool h[K];
-        uint64_t acc = 0;
-        bool any = false;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const uint32_t r = first + j;
-            v[j] = r < R ? (uint64_t)__ldcg(in + r) : 0;
-            h[j] = r < R && is_head(r);
-        }
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            if (h[j]) {
-                acc = 0;
-                any = true;
-            }
-            acc += v[j];
-            loc[j] = acc;
-        }
-        // (f, x): f = a segment starts inside, x = sum since the last start
-        uint32_t f = any;
-        uint64_t x = acc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t fu = __shfl_up_sync(0xffffffffu, f, o);
-            const uint64_t xu = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) {
-                if (!f) x += xu;
-                f |= fu;
-            }
-        }
-        if (lane == 31) {
-            sf[warp] = f;
-            sv[warp] = x;
-        }
-        // exclusive state within the warp
-        uint32_t fe = __shfl_up_sync(0xffffffffu, f, 1);
-        uint64_t xe = __shfl_up_sync(0xffffffffu, x, 1);
-        if (lane == 0) {
-            fe = 0;
-            xe = 0;
-        }
-        __syncthreads();
-        // prefix: carry, then earlier warps, then earlier lanes
-        uint32_t pf = 0;
-        uint64_t px = carry_v;
-        for (int w = 0; w < warp; ++w) {
-            px = sf[w] ? sv[w] : px + sv[w];
-            pf |= sf[w];
-        }
-        px = fe ? xe : px + xe;
-        bool seen = false;
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            seen = seen || h[j];
-            const uint32_t r = first + j;
-            if (r < R) out[r] = (seen ? 0 : px) + loc[j] - v[j];
-        }
-        // state after the whole tile, for the next one
-        uint64_t tx = carry_v;
-        for (int w = 0; w < kThreads / 32; ++w) tx = sf[w] ? sv[w] : tx + sv[w];
-        __syncthreads();
-        carry_v = tx;
-        (void)pf;
-    }
 }
 
 }  // namespace zccl

@@ -10,17 +10,21 @@
 // GB300 design.
 //
 //  escape_scan_kernel (used by the fused reduction, zccl_reduce.cu)  reads only the code planes (3/8 byte per element).
-//    One CTA per range of 32 chunks: each warp counts the escapes of 8 chunks
-//    with 16-byte loads (all issued first) and popc of ~(p0|p1|p2), and the
-//    CTA records each chunk's count, the escapes before each of its quarters
-//    (1024 slots: the share of one reducing warp) and its prefix within the
-//    range, plus the range total.  No CTA waits for another: the CTA that finishes last (an
-//    atomic arrival counter) runs one segmented exclusive scan over the range
-//    totals -- the inverse of the encoder's device-wide scan -- and checks
-//    each stream's total against its header.  It serves S streams at once
-//    for the fused reduction.  It is launched as a programmatic dependent of
-//    the preceding work and waits for it first, so its launch overlaps that
-//    work's tail.
+//    One CTA per range of 32 chunks, taken by ticket (an atomic counter, so
+//    every range below a CTA's own was taken by a CTA already running, in
+//    whatever order the hardware starts CTAs): each warp counts the escapes of 8 chunks
+//    with 16-byte loads (two chunks' loads issued at once) and popc of
+//    ~(p0|p1|p2), and the CTA records each chunk's count, the escapes before
+//    each of its quarters (1024 slots: the share of one reducing warp) and
+//    its prefix within the range.  The range's offset in its stream -- the
+//    inverse of the encoder's device-wide scan -- comes from a decoupled
+//    look-back: the CTA publishes the range total at once, then warp 0 reads
+//    the words of the ranges before it, nearest first, 32 at a time, and adds
+//    totals until it meets a published inclusive prefix; it then publishes
+//    its own.  The CTA of a stream's last range checks the stream's total
+//    against its header.  It serves S streams at once for the fused
+//    reduction.  It is launched as a programmatic dependent of the preceding
+//    work and waits for it first, so its launch overlaps that work's tail.
 //  decompress_kernel  one cooperative kernel with no grid barrier: each CTA
 //    counts the escapes of its own run of chunks from their planes and
 //    publishes the run total as a flag word, sums the earlier runs' totals
@@ -50,12 +54,10 @@ constexpr int kThreads = 128;
 // Kernel 1: escape offsets from the code planes
 // ============================================================================
 struct __align__(16) ScanSmem {
-    uint64_t scan64[kThreads / 32];
     uint64_t qinfo[kRangeChunks];
     uint32_t scan[kThreads / 32];
-    uint32_t scan_f[kThreads / 32];
+    uint64_t range;  // the range being counted (thread 0's ticket)
     uint32_t hdr_ok;
-    uint32_t last;
 };
 
 // The scan's header check: a 16-byte aligned stream whose header and blocks
@@ -138,6 +140,55 @@ __device__ __forceinline__ uint64_t warp_chunk_quarters(const uint4 (&p)[3], con
     return q0 | ((q0 + q1) << 16) | ((q0 + q1 + q2) << 32) | ((q0 + q1 + q2 + q3) << 48);
 }
 
+// Warp 0 of the CTA scanning range r, whose stream's ranges start at r0 < r:
+// the escapes of ranges r0 .. r - 1.  Lane i reads the look-back word of
+// range j - i (j = r - 1, r - 33, ...), waiting (bounded) until it is
+// published; the window's words up to the nearest inclusive prefix are
+// summed, and the walk stops there.  *ok is false if a wait timed out.
+__device__ uint64_t look_back(const uint64_t* lb, uint32_t r, uint32_t r0, bool* ok)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t sum = 0;
+    for (int64_t j = (int64_t)r - 1; j >= (int64_t)r0; j -= 32) {
+        const int64_t i = j - lane;
+        uint64_t w = kLbInclusive;  // before the stream's first range: an inclusive prefix of 0
+        bool mine = true;
+        if (i >= (int64_t)r0) w = poll_u64(lb + i, [](uint64_t v) { return (v & kLbState) != 0; }, &mine);
+        if (!__all_sync(0xffffffffu, mine)) {
+            *ok = false;
+            return 0;
+        }
+        const uint32_t inc = __ballot_sync(0xffffffffu, (w & kLbState) == kLbInclusive);
+        const int stop = inc ? __ffs(inc) - 1 : 31;
+        uint64_t v = lane <= stop ? (w & kLbValue) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        sum += v;
+        if (inc) break;
+    }
+    return sum;
+}
+
+// Checks stream s's header and that its escape count is `total` (the
+// recount from its planes); reports a mismatch.
+__device__ __forceinline__ void check_stream_total(const ScanArgs& a, uint32_t s, uint64_t total)
+{
+    uint64_t n_esc = 0;
+    if (!stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc) || n_esc != total)
+        report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+}
+
+// Thread 0: a range ticket of the running call.  Every CTA draws the same
+// number of tickets, ceil(nr / gridDim.x), so a call makes exactly that many
+// times gridDim.x draws (tickets past the last range are skipped); the CTA
+// that draws the last ticket resets the counter.
+__device__ __forceinline__ uint64_t draw_range(WsCtrl* ctrl, uint64_t last)
+{
+    const uint64_t t = atomicAdd(&ctrl->sticket, 1ull);
+    if (t == last) st_relaxed_u64(reinterpret_cast<uint64_t*>(&ctrl->sticket), 0ull);
+    return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs a)
 {
     __shared__ ScanSmem sm;
@@ -147,13 +198,38 @@ __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs
     // stream: nothing is read before that work is complete and visible
     pdl_wait();
     const uint32_t rps = (units + kRangeChunks - 1) / kRangeChunks;  // ranges per stream
-    const uint32_t nr = rps * a.S;
+    const uint64_t nr = (uint64_t)rps * a.S;
+    if (nr == 0) {  // no chunks: every stream must hold no escapes
+        if (blockIdx.x == 0)
+            for (uint32_t s = tid; s < a.S; s += kThreads)
+                if (s != a.skip) check_stream_total(a, s, 0);
+        pdl_launch_dependents();
+        return;
+    }
 
-    for (uint32_t r = blockIdx.x; r < nr; r += gridDim.x) {
-        const uint32_t s = r / rps, q = r % rps;
+    // Ranges are taken by ticket: every range below a CTA's own was taken by
+    // a CTA that is already running, in whatever order the hardware starts
+    // CTAs, so the look-back never waits for a CTA that has not started.
+    // With more than one draw per CTA, the next is drawn while the current
+    // range is counted.
+    const uint64_t draws = (nr + gridDim.x - 1) / gridDim.x;
+    const uint64_t last = draws * gridDim.x - 1;
+    uint64_t next = 0;
+    if (tid == 0) sm.range = draw_range(a.ctrl, last);
+    __syncthreads();
+    for (uint64_t d = 0; d < draws; ++d) {
+        const uint64_t r = sm.range;
+        if (tid == 0 && d + 1 < draws) next = draw_range(a.ctrl, last);
+        if (r >= nr) {  // a ticket past the last range (the same for the whole CTA)
+            __syncthreads();
+            if (tid == 0) sm.range = next;
+            __syncthreads();
+            continue;
+        }
+        const uint32_t s = (uint32_t)(r / rps), q = (uint32_t)(r % rps);
         // Counting needs only that the stream's blocks are there; the header
-        // itself is checked once, by the CTA that scans the range totals (and
-        // again by the reduce kernel before it uses it).  (The plain BF16
+        // itself is checked by the CTA of the stream's last range (and again
+        // by the reduce kernel before it uses it).  (The plain BF16
         // position, if any, has no stream: zero counts.)
         if (tid == 0) {
             const uint8_t* base = scan_stream(a, s);
@@ -203,31 +279,27 @@ __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs
             a.local[(uint64_t)s * units + c0 + tid] = ex;
             a.qinfo[(uint64_t)s * units + c0 + tid] = qi;
         }
-        if (tid == 0) a.totals[r] = agg;
-        __syncthreads();
-    }
-    pdl_launch_dependents();
-    if (arrive_last(a.ctrl, &sm.last)) {
-        cta_segmented_exclusive_scan<kThreads, 8>(
-            a.totals, a.bases, nr, [&](uint32_t r) { return r % rps == 0; }, sm.scan64, sm.scan_f);
-        __syncthreads();
-        // every stream's recount must equal its header's escape count
-        for (uint32_t s = tid; s < a.S; s += kThreads) {
-            uint64_t n_esc = 0;
-            if (s == a.skip) continue;
-            if (!stream_header_ok(scan_stream(a, s), scan_in_bytes(a, s), a.n, &n_esc)) {
-                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            } else if (rps > 0) {
-                const uint32_t last = s * rps + rps - 1;
-                if (a.bases[last] + __ldcg(a.totals + last) != n_esc) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
-            } else if (n_esc != 0) {
-                report(a.status, ZCCL_ERR_CORRUPT_STREAM);
+        if (warp == 0) {
+            // publish the range's total at once (the stream's first range:
+            // its inclusive prefix), then look back for its offset
+            if (lane == 0) st_relaxed_u64(a.lookback + r, (q == 0 ? kLbInclusive : kLbAggregate) | agg);
+            bool waited = true;
+            const uint64_t base = q == 0 ? 0 : look_back(a.lookback, r, r - q, &waited);
+            if (lane == 0) {
+                if (!waited) report(a.status, ZCCL_ERR_TIMEOUT);
+                if (q != 0) st_relaxed_u64(a.lookback + r, kLbInclusive | (base + agg));
+                a.bases[r] = base;
+                if (q == rps - 1 && s != a.skip) check_stream_total(a, s, base + agg);
             }
         }
+        if (tid == 0) sm.range = next;
         __syncthreads();
-        // leave the totals at zero: every call on a workspace expects them so
-        for (uint32_t r = tid; r < nr; r += kThreads) a.totals[r] = 0;
     }
+    // The reduction may launch only now: launched while ranges are still
+    // looking back, its CTAs (which wait for this grid before reading
+    // anything) were measured to slow the look-back down more than their
+    // early start saves.
+    pdl_launch_dependents();
 }
 
 // ============================================================================

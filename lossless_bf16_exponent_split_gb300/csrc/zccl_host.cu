@@ -104,17 +104,17 @@ DecompressLayout decompress_layout(uint64_t units)
     return l;
 }
 
-// Decompression / reduction workspace, per stream: escape total per range |
+// Decompression / reduction workspace, per stream: look-back word per range |
 // range base | chunk prefix within its range | quarter word per chunk.
 struct ScanLayout {
-    uint64_t totals, bases, local, qinfo, total;
+    uint64_t lookback, bases, local, qinfo, total;
 };
 ScanLayout scan_layout(uint64_t units, uint64_t S)
 {
     const uint64_t R = S * ranges_of(units);
     ScanLayout l;
-    l.totals = kPrefixBytes;
-    l.bases = round_up(l.totals + 4 * R, 16);
+    l.lookback = kPrefixBytes;
+    l.bases = round_up(l.lookback + 8 * R, 16);
     l.local = round_up(l.bases + 8 * R, 16);
     l.qinfo = round_up(l.local + 4 * S * units, 16);
     l.total = round_up(l.qinfo + 8 * S * units, 256);
@@ -326,7 +326,7 @@ zccl_status_t reduce_impl(const void* const* d_streams, const uint64_t* d_in_byt
     sc.skip = d_local != nullptr ? local_pos : S;
     sc.n = n;
     sc.ctrl = reinterpret_cast<WsCtrl*>(d_ws);
-    sc.totals = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.totals);
+    sc.lookback = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.lookback);
     sc.bases = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.bases);
     sc.local = reinterpret_cast<uint32_t*>((uint8_t*)d_ws + l.local);
     sc.qinfo = reinterpret_cast<uint64_t*>((uint8_t*)d_ws + l.qinfo);
@@ -342,6 +342,7 @@ zccl_status_t reduce_impl(const void* const* d_streams, const uint64_t* d_in_byt
     a.n = n;
     a.ctrl = sc.ctrl;
     a.bases = sc.bases;
+    a.lookback = sc.lookback;
     a.local_off = sc.local;
     a.qinfo = sc.qinfo;
     a.status = d_status;

@@ -37,7 +37,7 @@ struct ScanArgs {
     uint32_t skip;               // a position holding plain BF16 (no stream), or S for none
     uint64_t n;
     WsCtrl* ctrl;
-    uint32_t* totals;            // [S][ranges per stream] escapes per range
+    uint64_t* lookback;          // [S][ranges per stream] look-back words (kLbState | value)
     uint64_t* bases;             // [S][ranges per stream] range offset in its stream
     uint32_t* local;             // [S][units] chunk offset within its range
     uint64_t* qinfo;             // [S][units] quarter word per chunk (quarter_before / quarter_end)
@@ -67,6 +67,7 @@ struct ReduceArgs {
     uint64_t n;
     WsCtrl* ctrl;
     uint64_t* bases;             // from the scan: [S][ranges per stream] (cleared by the last CTA)
+    uint64_t* lookback;          // from the scan: [S][ranges per stream] (cleared by the last CTA)
     uint32_t* local_off;         // [S][units] chunk prefix within its range (cleared by the CTA that read it)
     uint64_t* qinfo;             // [S][units] quarter words (cleared by the CTA that read them)
     uint32_t* status;

@@ -481,11 +481,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) reduce_kernel(const Redu
             a.local_off[(uint64_t)s * total + c] = 0;
             a.qinfo[(uint64_t)s * total + c] = 0;
         }
-    // the last CTA to finish clears the range bases: the workspace is left
-    // all zero past its control block and flag area
+    // the last CTA to finish clears the range bases and the scan's look-back
+    // words: the workspace is left all zero past its control block and flag
+    // area
     if (arrive_last(a.ctrl, &sm.last)) {
         const uint64_t nb = (uint64_t)a.S * ((total + kRangeChunks - 1) / kRangeChunks);
-        for (uint64_t i = tid; i < nb; i += kThreads) a.bases[i] = 0;
+        for (uint64_t i = tid; i < nb; i += kThreads) {
+            a.bases[i] = 0;
+            a.lookback[i] = 0;
+        }
     }
 }
 

@@ -2,9 +2,9 @@
 //
 // The codec kernels wait on two kinds of things: mbarriers that their own
 // TMA bulk copies complete, and -- inside the cooperative compress and
-// decompress launches -- counters and flag words that other CTAs of the
-// same launch write (the call's done counter, the run totals and the
-// per-chunk entry words).  Every such wait gives up after a time limit and
+// decompress launches and the escape scan -- counters and flag words that
+// other CTAs of the same launch write (the call's done counter, the run
+// totals, the per-chunk entry words and the per-range look-back words).  Every such wait gives up after a time limit and
 // reports ZCCL_ERR_TIMEOUT instead of hanging.  These kernels let a test
 // show that each path works without faulting anything: one thread waits,
 // with the very same routine, on something that never completes.

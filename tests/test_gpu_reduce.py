@@ -79,9 +79,24 @@ def test_reduce_rejects_corrupt_header(codec, off, val):
     assert oracle.decompress_status(streams[1], n)[0] == oracle.CORRUPT
     st, _ = gpu_reduce(codec, streams, n)
     assert st == 3
-    # the same workspace-free call path then reduces good shards exactly
+    # the same codec, on the same workspace, then reduces good shards exactly
     st, got = gpu_reduce(codec, good, n)
     assert st == 0 and np.array_equal(got, oracle.decompress_reduce(good, n))
+
+
+def test_reduce_more_ranges_than_scan_ctas(codec):
+    """1,024 shards (the most a call takes) of 131,073 elements: two ranges
+    of 32 chunks per stream, 2,048 ranges -- more than one per CTA of the
+    escape scan's grid (8 CTAs per SM), so its CTAs take several range
+    tickets each and the look-back spans ranges taken in different rounds."""
+    S, n = 1024, 32 * 4096 + 1
+    lut = oracle.lut_from_sigma(1.0)
+    shards = [workloads.special_values(n, seed=7000 + s, frac=0.01) for s in range(S)]
+    streams = [oracle.compress(x, lut) for x in shards]
+    want = oracle.decompress_reduce(streams, n)
+    st, got = gpu_reduce(codec, streams, n)
+    assert st == 0
+    assert np.array_equal(got, want)
 
 
 def test_rs_local_full(codec):
