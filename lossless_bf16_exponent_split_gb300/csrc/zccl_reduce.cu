@@ -64,14 +64,27 @@ constexpr uint32_t kZpCap = 512;                   // one 16-byte copy per lane:
 // to match.
 constexpr int kCtasPerSm = 6;
 static_assert(kZpOff % 16 == 0 && kZpOff + kZpCap <= kStageBytes, "the zero-point cover fits the stage");
+// The step window: a ring of kWin steps per warp, refilled kWinLoad at a time.
+constexpr uint32_t kWin = 32, kWinLoad = 16;
+// A step's info word: the escape count of the quarter (bits 0..12), the
+// bytes of its 16-byte aligned zero-point cover when that fits the stage
+// (bits 16..26; else 0), whether it does (bit 30), whether the offsets
+// passed the bounds checks (bit 31); bit 29 marks a plain BF16 step.
+constexpr uint32_t kInfoCount = 0x1FFFu, kInfoInStage = 1u << 30, kInfoOk = 1u << 31, kInfoPlain = 1u << 29;
+__device__ __forceinline__ uint32_t info_cover(uint32_t info) { return (info >> 16) & 0x7FFu; }
 
 struct __align__(128) ReduceSmem {
     uint8_t stage[kWarps][kStages][kStageBytes];
     uint8_t xe[kWarps][kQuarter];  // each lane's escaped exponents (rotated), 32 bytes
     uint32_t spread[3][256];       // spread_nibbles(b) << p, p = plane
-    // per warp, two windows of 32 steps: the quarter's first zero-point
-    // offset and its escape count
-    uint64_t win[kWarps][2 * 32][2];
+    // Per warp, a ring of kWin steps (two halves of kWinLoad): each step's
+    // copy sources and checks, computed ahead by the warp's lanes, one step
+    // each (load_window).  wptr: the quarter's first source byte (a stream
+    // step: its sign-mantissa bytes; a plain step: its BF16) and the first
+    // byte of its zero-point run; winfo: a stream step's plane size L / 8
+    // (a plain step: its valid slots) and the info word (kInfo*).
+    uint64_t wptr[kWarps][kWin][2];
+    uint32_t winfo[kWarps][kWin][2];
     uint32_t last;
 };
 // followed by per-shard tables: blk[S], zpa[S], n_esc[S] (8 bytes each), lut[S] (uint2)
@@ -191,32 +204,53 @@ __device__ __forceinline__ void decode_add8(float2* acc, uint32_t N, uint2 smb, 
     add_bf16x2(acc[3], __byte_perm(lo_b, hi_b, 0x7362));
 }
 
-// One warp: the zero-point offset and escape count of its quarter in steps
-// w .. w + 31 (lane i: step w + i) into window slot (w / 32) & 1 of the
-// warp.  The loads are waited for here: it happens once per 32 steps.
+// One warp: the window entries of its steps w .. w + kWinLoad - 1 (lane i:
+// step w + i), into half (w / kWinLoad) & 1 of its ring.  All the per-step
+// address arithmetic and bounds checks happen here, a step per lane; the
+// loads are waited for here, once per kWinLoad steps.
 template <bool kPlain>
-__device__ __forceinline__ void load_window(const ReduceArgs& a, ReduceSmem& sm, uint32_t w, uint32_t steps)
+__device__ __forceinline__ void load_window(const ReduceArgs& a, ReduceSmem& sm, const ShardTables& t, uint32_t w,
+                                            uint32_t steps)
 {
     const uint32_t lane = threadIdx.x & 31, q = threadIdx.x >> 5, step = w + lane;
+    if (lane >= kWinLoad) return;
     const uint32_t total = (uint32_t)units_of(a.n);
     const uint32_t Q = steps_per_chunk<kPlain>(a);
-    uint64_t zq = 0, cnt = 0;
+    uint64_t src = 0, zsrc = 0;
+    uint32_t l8 = 0, info = 0;
     if (step < steps) {
         const uint32_t k = step / Q, sq = step - k * Q;
+        const uint64_t c = blockIdx.x + (uint64_t)k * gridDim.x;
+        const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - c * kChunk);
         uint32_t s = 0;
-        if (step_kind<kPlain>(a, sq, &s) == kStepStream) {
-            const uint64_t c = blockIdx.x + (uint64_t)k * gridDim.x;
+        const uint32_t kind = step_kind<kPlain>(a, sq, &s);
+        if (kind == kStepStream) {
+            const uint32_t L = slots_of(valid);
             const uint32_t rps = (total + kRangeChunks - 1) / kRangeChunks;
             const uint64_t qi = __ldcg(a.qinfo + (uint64_t)s * total + c);
             const uint32_t before = quarter_before(qi, q);
-            zq = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks) +
-                 __ldcg(a.local_off + (uint64_t)s * total + c) + before;
-            cnt = quarter_end(qi, q) - before;
+            const uint64_t zq = __ldcg(a.bases + (uint64_t)s * rps + c / kRangeChunks) +
+                                __ldcg(a.local_off + (uint64_t)s * total + c) + before;
+            const uint32_t cnt = quarter_end(qi, q) - before;
+            src = reinterpret_cast<uint64_t>(t.blk[s] + c * kBlockBytes + q * kQuarter);
+            l8 = L / 8;
+            if (cnt <= kQuarter && zq + cnt <= t.n_esc[s]) {
+                zsrc = reinterpret_cast<uint64_t>(t.zpa[s] + zq);
+                const uint32_t cover = (((uint32_t)zsrc & 15u) + cnt + 15u) & ~15u;
+                info = cnt | kInfoOk | (cover <= kZpCap ? (cover << 16) | kInfoInStage : 0u);
+            }
+        } else {
+            const uint16_t* base = kind == kStepLocal ? a.local : a.out;
+            src = reinterpret_cast<uint64_t>(base + c * kChunk + q * kQuarter);
+            l8 = min(kQuarter, valid - q * kQuarter);
+            info = kInfoPlain;
         }
     }
-    const uint32_t e = smem_addr(sm.win[q][((w / 32) & 1) * 32 + lane]);
-    sts_u64(e, zq);
-    sts_u64(e + 8, cnt);
+    const uint32_t e = ((w / kWinLoad) & 1) * kWinLoad + lane;
+    sts_u64(smem_addr(&sm.wptr[q][e][0]), src);
+    sts_u64(smem_addr(&sm.wptr[q][e][1]), zsrc);
+    sts_u32(smem_addr(&sm.winfo[q][e][0]), l8);
+    sts_u32(smem_addr(&sm.winfo[q][e][1]), info);
 }
 
 // One warp: its quarter q of the CTA's chunks blockIdx.x + k * gridDim.x,
@@ -242,60 +276,50 @@ __device__ __forceinline__ void reduce_quarters(const ReduceArgs& a, ReduceSmem&
     const uint32_t steps = units * Q;
     const uint32_t stage0 = smem_addr(sm.stage[q][0]);
 
-    load_window<kPlain>(a, sm, 0, steps);
-    load_window<kPlain>(a, sm, 32, steps);
+    load_window<kPlain>(a, sm, t, 0, steps);
+    load_window<kPlain>(a, sm, t, kWinLoad, steps);
     __syncwarp();
 
-    // Issue cursor: step ij, unit ik, step is within it, into stage ist.
-    // Every lane copies; each step is one cp.async group of every lane
-    // (empty past the last step, so that the group count stays uniform).
-    uint32_t ij = 0, ik = 0, is = 0, ist = 0;
+    // lane constants of the copies: this lane's piece of the planes (lanes
+    // 0..23: 16 bytes of plane lane / 8), at src + (8 + lane / 8) * L / 8 +
+    // 16 (lane % 8) - 896 q from the quarter's first sign-mantissa byte
+    const uint32_t pmul = 8 + (lane >> 3);
+    const uint32_t pconst = 16 * (lane & 7) - (kQuarter - kPlaneBytes) * q;
+    const uint32_t wp0 = smem_addr(&sm.wptr[q][0][0]), wi0 = smem_addr(&sm.winfo[q][0][0]);
+
+    // Issue cursor: step ij into stage ist.  Every lane copies; each step is
+    // one cp.async group of every lane (empty past the last step, so that
+    // the group count stays uniform).
+    uint32_t ij = 0, ist = 0;
     auto issue = [&]() {
         if (ij < steps) {
-            // mid-window: the next window (its slot held steps all consumed by now)
-            if ((ij & 31) == 16) {
-                load_window<kPlain>(a, sm, (ij & ~31u) + 32, steps);
+            // the next half of the window: it held steps all consumed by now
+            if ((ij & (kWinLoad - 1)) == kWinLoad / 2 && ij >= kWinLoad) {
+                load_window<kPlain>(a, sm, t, (ij & ~(kWinLoad - 1)) + kWinLoad, steps);
                 __syncwarp();
             }
-            const uint64_t c = blockIdx.x + (uint64_t)ik * G;
-            const uint32_t valid = unit_valid(ik);
+            const uint32_t e = ij & (kWin - 1);
+            const uint4 wp = lds_u128(wp0 + 16 * e);
+            const uint2 wi = lds_u64(wi0 + 8 * e);
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(((uint64_t)wp.y << 32) | wp.x);
             const uint32_t dst = stage0 + ist * kStageBytes;
-            uint32_t s = 0;
-            const uint32_t kind = step_kind<kPlain>(a, is, &s);
-            if (kind != kStepStream) {  // plain BF16: the lane's whole 16-byte pieces, the rest by plain loads
-                const uint32_t vq = min(kQuarter, valid - q * kQuarter);
-                const uint16_t* src = (kind == kStepLocal ? a.local : a.out) + c * kChunk + q * kQuarter;
+            if (kPlain && (wi.y & kInfoPlain)) {  // plain BF16: the lane's whole 16-byte pieces, the rest by plain loads
 #pragma unroll
                 for (uint32_t k = 0; k < 4; ++k) {
                     const uint32_t e0 = 32 * lane + 8 * k;  // the piece's first element
-                    if (e0 + 8 <= vq) cp_async16(dst + 2 * e0, src + e0);
+                    if (e0 + 8 <= wi.x) cp_async16(dst + 2 * e0, src + 2 * e0);
                 }
             } else {
-                const uint32_t L = slots_of(valid);
-                const uint8_t* blk = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * s)) + c * kBlockBytes;
                 // the lane's sign-mantissa bytes
-                cp_async16(dst + 32 * lane, blk + q * kQuarter + 32 * lane);
-                cp_async16(dst + 32 * lane + 16, blk + q * kQuarter + 32 * lane + 16);
-                // lanes 0..23: 16 bytes of plane lane / 8
-                if (lane < 24) {
-                    const uint32_t p = lane >> 3, piece = 16 * (lane & 7);
-                    cp_async16(dst + kPlaneOff + p * kPlaneBytes + piece, blk + L + p * (L / 8) + q * kPlaneBytes + piece);
-                }
+                cp_async16(dst + 32 * lane, src + 32 * lane);
+                cp_async16(dst + 32 * lane + 16, src + 32 * lane + 16);
+                if (lane < 24) cp_async16(dst + kPlaneOff + 16 * lane, src + (pmul * wi.x + pconst));
                 // the quarter's zero points: its 16-byte aligned cover, one piece per lane
-                const uint32_t wa = smem_addr(sm.win[q][ij & 63]);
-                const uint64_t zq = lds_u64w(wa);
-                const uint32_t cnt = (uint32_t)lds_u64w(wa + 8);
-                const bool ok = cnt <= kQuarter && zq + cnt <= lds_u64w(tab + 16 * S + 8 * s);
-                const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * S + 8 * s)) + zq;
-                const uint32_t zmis = (uint32_t)(uintptr_t)zsrc & 15u;
-                const uint32_t cover = (zmis + cnt + 15u) & ~15u;
-                if (ok && cover <= kZpCap && 16 * lane < cover) cp_async16(dst + kZpOff + 16 * lane, zsrc - zmis + 16 * lane);
+                const uint64_t z = ((uint64_t)wp.w << 32) | wp.z;
+                if (16 * lane < info_cover(wi.y))
+                    cp_async16(dst + kZpOff + 16 * lane, reinterpret_cast<const uint8_t*>((z & ~15ull) + 16 * lane));
             }
             ++ij;
-            if (++is == Q) {
-                is = 0;
-                ++ik;
-            }
             if (++ist == kStages) ist = 0;
         }
         cp_async_commit();
@@ -345,16 +369,14 @@ __device__ __forceinline__ void reduce_quarters(const ReduceArgs& a, ReduceSmem&
                     if (lane >= (uint32_t)o) incl += y;
                 }
                 const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-                const uint32_t wa = smem_addr(sm.win[q][j & 63]);
-                const uint64_t zq = lds_u64w(wa);
-                const uint32_t cnt = (uint32_t)lds_u64w(wa + 8);
-                const bool ok = cnt <= kQuarter && zq + cnt <= lds_u64w(tab + 16 * S + 8 * s);
-                if (ok && tot == cnt) {
+                const uint32_t e = j & (kWin - 1);
+                const uint32_t info = lds_u32(wi0 + 8 * e + 4);
+                if ((info & kInfoOk) && tot == (info & kInfoCount)) {
                     if (esc) {
-                        const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(lds_u64w(tab + 8 * S + 8 * s)) + zq;
+                        const uint8_t* zsrc = reinterpret_cast<const uint8_t*>(lds_u64w(wp0 + 16 * e + 8));
                         const uint32_t zmis = (uint32_t)(uintptr_t)zsrc & 15u;
                         uint32_t m = esc;
-                        if (((zmis + cnt + 15u) & ~15u) <= kZpCap) {  // the run is in the stage
+                        if (info & kInfoInStage) {  // the run is in the stage
                             const uint32_t src = stg + kZpOff + zmis + (incl - ne);
                             for (uint32_t r = 0; m; ++r) {
                                 const uint32_t b = __ffs(m) - 1;
