@@ -110,10 +110,15 @@ __device__ __forceinline__ ShardTables shard_tables(uint8_t* smem_raw, uint32_t 
     return t;
 }
 
-// An exponent byte rotated right by one bit: bit 7 = exponent bit 0, bits
-// 0..6 = exponent >> 1 -- the low and high byte of a BF16 value then each
-// take one masked merge with the sign-mantissa byte.
-__device__ __forceinline__ uint32_t rot_exp(uint32_t e) { return ((e >> 1) | (e << 7)) & 0xFFu; }
+// Exponent bytes are held rotated right by one bit: bit 7 = exponent bit 0,
+// bits 0..6 = exponent >> 1 -- the low and high byte of a BF16 value then
+// each take one masked merge with the sign-mantissa byte.
+//
+// One exponent byte e rotated, in the low byte only (bits above it are
+// garbage), for a byte store: e * 257 = e | e << 8 for e < 256, and a shift
+// right by one brings bit 0 of the low copy under bit 7.  One multiply-add
+// and one shift.
+__device__ __forceinline__ uint32_t rot_exp_lo8(uint32_t e) { return (e * 257u) >> 1; }
 __device__ __forceinline__ uint32_t rot_exp4(uint32_t w) { return ((w >> 1) & 0x7F7F7F7Fu) | ((w << 7) & 0x80808080u); }
 
 // The steps of an output chunk: (accumulating) the output's current values,
@@ -381,14 +386,14 @@ __device__ __forceinline__ void reduce_quarters(const ReduceArgs& a, ReduceSmem&
                             for (uint32_t r = 0; m; ++r) {
                                 const uint32_t b = __ffs(m) - 1;
                                 m &= m - 1;
-                                sts_u8(xa + (b ^ xsw), rot_exp(lds_u8(src + r)));
+                                sts_u8(xa + (b ^ xsw), rot_exp_lo8(lds_u8(src + r)));
                             }
                         } else {  // a run too long for the stage: read in place
                             const uint8_t* src = zsrc + (incl - ne);
                             for (uint32_t r = 0; m; ++r) {
                                 const uint32_t b = __ffs(m) - 1;
                                 m &= m - 1;
-                                sts_u8(xa + (b ^ xsw), rot_exp(__ldg(src + r)));
+                                sts_u8(xa + (b ^ xsw), rot_exp_lo8(__ldg(src + r)));
                             }
                         }
                     }
