@@ -12,9 +12,10 @@
 //  escape_scan_kernel (used by the fused reduction, zccl_reduce.cu)  reads only the code planes (3/8 byte per element).
 //    One CTA per range of 32 chunks, taken by ticket (an atomic counter, so
 //    every range below a CTA's own was taken by a CTA already running, in
-//    whatever order the hardware starts CTAs): each warp counts the escapes of 8 chunks
-//    with 16-byte loads (two chunks' loads issued at once) and popc of
-//    ~(p0|p1|p2), and the CTA records each chunk's count, the escapes before
+//    whatever order the hardware starts CTAs): each warp counts the escapes
+//    of 8 chunks with 16-byte loads (the next two chunks' loads in flight
+//    while one is counted) and popc of ~(p0|p1|p2), and the CTA records each
+//    chunk's count, the escapes before
 //    each of its quarters (1024 slots: the share of one reducing warp) and
 //    its prefix within the range.  The range's offset in its stream -- the
 //    inverse of the encoder's device-wide scan -- comes from a decoupled
@@ -189,7 +190,7 @@ __device__ __forceinline__ uint64_t draw_range(WsCtrl* ctrl, uint64_t last)
     return t;
 }
 
-__global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs a)
+__global__ void __launch_bounds__(kThreads, 7) escape_scan_kernel(const ScanArgs a)
 {
     __shared__ ScanSmem sm;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -241,32 +242,34 @@ __global__ void __launch_bounds__(kThreads, 8) escape_scan_kernel(const ScanArgs
         const uint32_t nch = min(kRangeChunks, units - c0);
         const bool ok = sm.hdr_ok != 0;
         if (ok) {
-            // each warp counts 8 chunks, 2 at a time: the planes of a batch's
-            // full chunks are loaded first (6 16-byte loads in flight per lane)
-            constexpr int kBatch = 2;
+            // each warp counts 8 chunks, one at a time, the planes of the
+            // next two chunks in flight while one is counted
             const uint8_t* base = scan_stream(a, s);
-#pragma unroll 1
-            for (int b = 0; b < kRangeChunks / (kThreads / 32) / kBatch; ++b) {
-                uint4 p[kBatch][3];
+            auto load = [&](uint32_t i, uint4 (&p)[3]) {
+                const uint64_t c = c0 + i;
+                if (i < nch && (c + 1) * kChunk <= a.n) {
+                    const uint4* pw = reinterpret_cast<const uint4*>(base + kHeaderBytes + c * kBlockBytes + kChunk);
 #pragma unroll
-                for (int ii = 0; ii < kBatch; ++ii) {
-                    const uint32_t i = warp + 4 * (kBatch * b + ii);
+                    for (int qq = 0; qq < 3; ++qq) p[qq] = __ldg(pw + qq * 32 + lane);
+                }
+            };
+            uint4 pa[3], pb[3], pc[3];
+            load(warp, pa);
+            load(warp + 4, pb);
+#pragma unroll
+            for (int b = 0; b < kRangeChunks / (kThreads / 32); ++b) {
+                const uint32_t i = warp + 4 * b;
+                if (b + 2 < kRangeChunks / (kThreads / 32)) load(i + 8, pc);
+                if (i < nch) {
                     const uint64_t c = c0 + i;
-                    if (i < nch && (c + 1) * kChunk <= a.n) {
-                        const uint4* pw =
-                            reinterpret_cast<const uint4*>(base + kHeaderBytes + c * kBlockBytes + kChunk);
-#pragma unroll
-                        for (int qq = 0; qq < 3; ++qq) p[ii][qq] = __ldg(pw + qq * 32 + lane);
-                    }
+                    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - c * kChunk);
+                    const uint64_t qi = warp_chunk_quarters(pa, base + kHeaderBytes + c * kBlockBytes, valid);
+                    if (lane == 0) sm.qinfo[i] = qi;
                 }
 #pragma unroll
-                for (int ii = 0; ii < kBatch; ++ii) {
-                    const uint32_t i = warp + 4 * (kBatch * b + ii);
-                    const uint64_t c = c0 + i;
-                    if (i >= nch) continue;
-                    const uint32_t valid = (uint32_t)min((uint64_t)kChunk, a.n - c * kChunk);
-                    const uint64_t qi = warp_chunk_quarters(p[ii], base + kHeaderBytes + c * kBlockBytes, valid);
-                    if (lane == 0) sm.qinfo[i] = qi;
+                for (int qq = 0; qq < 3; ++qq) {
+                    pa[qq] = pb[qq];
+                    pb[qq] = pc[qq];
                 }
             }
         }
