@@ -24,6 +24,11 @@
 // quarter's run of the zero-point array.  A step waits for its own copies
 // (cp.async.wait_group) and then for the warp's (a warp barrier).  No warp
 // ever waits for another, and no single thread issues copies for others.
+// Every per-step address and check (the step's shard and chunk, its source
+// bytes, its zero-point offset, count and cover, the bounds checks) is
+// computed ahead by the warp's lanes, one step each, 16 steps at a time,
+// into a 32-step ring in shared memory: a step's copy issue is two shared
+// loads and per-lane constant offsets.
 // Lane l owns slots [32 l, 32 l + 32) of the quarter, i.e. one word of each
 // code plane: after a warp scan of the escape counts it places its own
 // escaped exponents, then decodes its 32 elements straight into fp32 sums
@@ -40,7 +45,7 @@
 // fp32 x (including +0, -0, subnormals, infinities and NaN), so every shard,
 // the first included, is one add and no step needs a separate first form.
 // The adds widen BF16 to fp32 inside the add instruction (exact), so a
-// packed pair of BF16 values feeds two adds with no unpacking.
+// packed pair of BF16 values feeds two adds directly.
 #include <cstdint>
 
 #include "zccl_common.cuh"
