@@ -84,6 +84,26 @@ def test_reduce_rejects_corrupt_header(codec, off, val):
     assert st == 0 and np.array_equal(got, oracle.decompress_reduce(good, n))
 
 
+def test_reduce_empty_streams(codec):
+    """n = 0: every stream is a bare header, the output is empty and the
+    status stays 0.  A header that claims one escape is rejected as the
+    oracle rejects it -- whether the zero-point array it promises is missing
+    (the size check) or present (128 zero bytes: the recount of 0 escapes
+    disagrees with the header)."""
+    lut = oracle.lut_from_sigma(1.0)
+    empty = [oracle.compress(np.zeros(0, np.uint16), lut) for _ in range(3)]
+    st, got = gpu_reduce(codec, empty, 0)
+    assert st == 0 and got.size == 0
+    claim = bytearray(empty[1])
+    claim[16] = 1  # n_esc = 1
+    for bad in (bytes(claim), bytes(claim) + bytes(128)):
+        assert oracle.decompress_status(bad, 0)[0] == oracle.CORRUPT
+        st, got = gpu_reduce(codec, [empty[0], bad, empty[2]], 0)
+        assert st == 3 and got.size == 0
+    st, _ = gpu_reduce(codec, empty, 0)  # the workspace is ready again
+    assert st == 0
+
+
 def test_reduce_more_ranges_than_scan_ctas(codec):
     """1,024 shards (the most a call takes) of 131,073 elements: two ranges
     of 32 chunks per stream, 2,048 ranges -- more than one per CTA of the
