@@ -146,7 +146,7 @@ __device__ __forceinline__ uint64_t warp_chunk_quarters(const uint4 (&p)[3], con
 // range j - i (j = r - 1, r - 33, ...), waiting (bounded) until it is
 // published; the window's words up to the nearest inclusive prefix are
 // summed, and the walk stops there.  *ok is false if a wait timed out.
-__device__ uint64_t look_back(const uint64_t* lb, uint32_t r, uint32_t r0, bool* ok)
+__device__ uint64_t look_back(const uint64_t* lb, uint64_t r, uint64_t r0, bool* ok)
 {
     const int lane = threadIdx.x & 31;
     uint64_t sum = 0;
