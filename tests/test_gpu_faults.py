@@ -138,9 +138,10 @@ def test_workspace_reused_across_many_calls(z):
 
 @pytest.mark.parametrize("kind", ["counter", "flag"])
 def test_bounded_polls_report_timeout(z, kind):
-    """The cooperative kernels also wait on words other CTAs write: the call's
-    done counter (compress and decompress) and the run-total and chunk-entry
-    flag words (decompress).  zccl_check_bounded_poll runs those same waits
+    """The kernels also wait on words other CTAs write: the call's done
+    counter (compress and decompress), the run-total and chunk-entry flag
+    words (decompress) and the look-back words of earlier ranges (the escape
+    scan of decompress-reduce).  zccl_check_bounded_poll runs those same waits
     on a zeroed word that nothing ever sets: each must end (after 3 ms) with
     ZCCL_ERR_TIMEOUT, and the context must stay usable."""
     k = z.POLL_COUNTER if kind == "counter" else z.POLL_FLAG
