@@ -100,8 +100,30 @@ struct __align__(16) CompressSmem {
     uint32_t calls;
     uint32_t next[2];  // the chunk of iteration k + 1, in next[(k + 1) & 1]: slow threads
                        // still read one slot while thread 0 fills the other
+    uint32_t nseg[2];  // ... and its segment
 };
-// followed by ustart[n_segs + 1]: first global chunk of each segment
+// followed by ustart[n_segs + 1]: first global chunk of each segment, and
+// (up to kSegCache segments) each segment's input address and length, so
+// that the per-chunk lookups stay in shared memory
+constexpr uint32_t kSegCache = 128;
+__device__ __forceinline__ uint64_t* seg_cache(uint32_t* ustart, uint32_t n_segs)
+{
+    return reinterpret_cast<uint64_t*>(ustart + ((n_segs + 2) & ~1u));  // 8-byte aligned: in[n_segs], n[n_segs]
+}
+// A segment's input address and length.
+struct SegIn {
+    const uint16_t* in;
+    uint64_t n;
+};
+__device__ __forceinline__ SegIn seg_in(const CompressArgs& a, const uint32_t* ustart, uint32_t s)
+{
+    if (a.n_segs <= kSegCache) {
+        const uint64_t* sc = seg_cache(const_cast<uint32_t*>(ustart), a.n_segs);
+        return SegIn{reinterpret_cast<const uint16_t*>(sc[s]), sc[a.n_segs + s]};
+    }
+    const zccl_segment_t d = seg_get(a, s);
+    return SegIn{d.in, d.n};
+}
 
 // Per-segment first chunk in shared memory (invalid segments get no chunks);
 // returns the total chunk count.  All threads; contains barriers.
@@ -114,6 +136,11 @@ __device__ uint64_t segment_table(const CompressArgs& a, uint32_t* ustart, uint6
         if (s < a.n_segs) {
             const zccl_segment_t d = seg_get(a, s);
             if (a.segs == nullptr || segment_error(d) == 0) u = units_of(d.n);
+            if (a.n_segs <= kSegCache) {
+                uint64_t* sc = seg_cache(ustart, a.n_segs);
+                sc[s] = reinterpret_cast<uint64_t>(d.in);
+                sc[a.n_segs + s] = d.n;
+            }
         }
         uint64_t tot;
         const uint64_t ex = block_exclusive_scan<kThreads, uint64_t>(u, scan64, &tot);
@@ -125,11 +152,12 @@ __device__ uint64_t segment_table(const CompressArgs& a, uint32_t* ustart, uint6
     return run;
 }
 
-__device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, CompressSmem& sm,
-                                                 uint32_t c, int buf)
+// Thread 0: starts the load of chunk c into buffer buf; returns its segment.
+__device__ __forceinline__ uint32_t issue_chunk_load(const CompressArgs& a, const uint32_t* ustart, CompressSmem& sm,
+                                                     uint32_t c, int buf)
 {
     const uint32_t s = find_segment(ustart, a.n_segs, c);
-    const zccl_segment_t d = seg_get(a, s);
+    const SegIn d = seg_in(a, ustart, s);
     const uint64_t first = (uint64_t)(c - ustart[s]) * kChunk;
     const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
     const uint32_t bytes = (valid * 2) & ~15u;  // whole 16-byte pieces; the rest by plain loads
@@ -139,6 +167,7 @@ __device__ __forceinline__ void issue_chunk_load(const CompressArgs& a, const ui
     } else {
         mbar_arrive(&sm.bar[buf]);
     }
+    return s;
 }
 
 // Header of a finished stream (the 32 lanes of one warp write 4 bytes each).
@@ -169,7 +198,7 @@ __device__ __forceinline__ void write_header(uint8_t* out, uint64_t n, uint64_t 
 // the block and plane offsets are constants and no lane masks its tail.
 template <bool kFull>
 __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSmem& sm, int buf, uint32_t c,
-                                               const zccl_segment_t& d, uint32_t cl, uint32_t valid_arg,
+                                               uint8_t* out, uint32_t cl, uint32_t valid_arg,
                                                bool timed_out)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -218,7 +247,7 @@ __device__ __forceinline__ uint32_t code_chunk(const CompressArgs& a, CompressSm
     // some thread's bounded wait, nothing is stored)
     if (__syncthreads_or(timed_out)) return kAborted;
     if (tid == 0) {
-        bulk_s2g((uint8_t*)d.out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
+        bulk_s2g(out + kHeaderBytes + (uint64_t)cl * kBlockBytes, sm.blk, L * 11 / 8);
         bulk_commit();
     }
     // escapes: words from the planes, chunk-local compaction into the stage
@@ -299,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         const uint32_t t = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
         sm.next[0] = t;
         if (t < T) {
-            issue_chunk_load(a, ustart, sm, t, 0);
+            sm.nseg[0] = issue_chunk_load(a, ustart, sm, t, 0);
             tn_pf = draw_ticket(a.ctrl);
         }
     }
@@ -311,13 +340,16 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
             const uint32_t tn = consume_ticket(a.ctrl, tn_pf, T);
             sm.next[(k + 1) & 1] = tn;
             if (tn < T) {
-                issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
+                sm.nseg[(k + 1) & 1] = issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
                 tn_pf = draw_ticket(a.ctrl);
             }
             if (k == 0) sm.calls = calls;  // for the bookkeeper, after the first chunk
         }
-        const uint32_t s = find_segment(ustart, a.n_segs, c);
-        const zccl_segment_t d = seg_get(a, s);
+        const uint32_t s = sm.nseg[k & 1];  // (found by thread 0 when it started the load)
+        const SegIn d = seg_in(a, ustart, s);
+        // the output address only for thread 0's block store (read now,
+        // used after the coding)
+        uint8_t* out = tid == 0 ? (uint8_t*)seg_get(a, s).out : nullptr;
         const uint32_t cl = c - ustart[s];
         const uint64_t first = (uint64_t)cl * kChunk;
         const uint32_t valid = (uint32_t)umin64(kChunk, d.n - first);
@@ -328,8 +360,8 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
                 reinterpret_cast<uint16_t*>(sm.in[buf])[done + tid] = d.in[first + done + tid];
             __syncthreads();
         }
-        const uint32_t agg = valid == kChunk ? code_chunk<true>(a, sm, buf, c, d, cl, valid, timed_out)
-                                             : code_chunk<false>(a, sm, buf, c, d, cl, valid, timed_out);
+        const uint32_t agg = valid == kChunk ? code_chunk<true>(a, sm, buf, c, out, cl, valid, timed_out)
+                                             : code_chunk<false>(a, sm, buf, c, out, cl, valid, timed_out);
         if (agg == kAborted) {  // a bulk load never landed (bounded wait ran out)
             if (tid == 0) {
                 sm.abort = 1;
@@ -525,7 +557,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
 
 }  // namespace
 
-size_t compress_smem_bytes(uint32_t n_segs) { return sizeof(CompressSmem) + 4ull * (n_segs + 1); }
+size_t compress_smem_bytes(uint32_t n_segs)
+{
+    return sizeof(CompressSmem) + 4ull * ((n_segs + 2) & ~1u) + (n_segs <= kSegCache ? 16ull * n_segs : 0ull);
+}
 
 cudaError_t launch_compress(const CompressArgs& a, uint32_t grid, cudaStream_t stream)
 {
