@@ -87,9 +87,8 @@ __device__ __forceinline__ bool header_valid(const uint32_t* h, uint64_t in_byte
 // the call's count (all CTAs have read `calls` by then) advances `calls`.
 // Decompression draws chunk tickets from dticket[calls & 1] (it knows the
 // parity by then) and clears the other one; compression draws them from one
-// counter before it knows the parity: every CTA draws until it gets one
-// past the last chunk and then stops, so a call makes exactly chunks + CTAs
-// draws, and the CTA that drew the last of them resets the counter.  Calls
+// counter before it knows the parity, and the CTA whose add completes the
+// call's done count (every draw has returned by then) resets it.  Calls
 // on one workspace run in stream order, so a call never sees another call's
 // state.
 constexpr uint32_t kArrivalGroups = 32;
@@ -477,15 +476,40 @@ __device__ __forceinline__ void call_end(WsCtrl* ctrl, uint32_t calls, bool last
     if (last) st_relaxed_u32(&ctrl->calls, calls + 1);
 }
 
-// Thread 0 (compress): chunk tickets from one counter.  draw_ticket starts
-// a draw; the value is consumed (with consume_ticket) only when needed, so
-// the atomic's round trip does not stall the thread.  A CTA stops drawing
-// after it consumes its first ticket >= T, so a call makes exactly
-// T + gridDim.x draws; the one that drew the last resets the counter.
-__device__ __forceinline__ uint32_t draw_ticket(WsCtrl* ctrl) { return atomicAdd(&ctrl->ticket, 1u); }
-__device__ __forceinline__ uint32_t consume_ticket(WsCtrl* ctrl, uint32_t t, uint32_t T)
+// Thread 0: chunk tickets from one counter.  A ticket is a run of
+// consecutive chunks: 4 while at least 16 x gridDim.x chunks remain after it,
+// 2 while at least 4 x gridDim.x do, then 1, so the counter sees a quarter of
+// the draws for most of a large call and the tail still balances chunk by
+// chunk.  (With one draw per chunk, the counter's L2 slice could not keep up
+// under the call's own streaming traffic on some placements of the counter.)
+__device__ __forceinline__ uint32_t ticket_chunks(uint32_t remaining)
 {
-    if (t == T + gridDim.x - 1) st_relaxed_u32(&ctrl->ticket, 0u);
+    const uint32_t G = gridDim.x;
+    return remaining >= 16u * G ? 4u : (remaining >= 4u * G ? 2u : 1u);
+}
+// The first draw of a CTA: at least min_chunks chunks.
+__device__ __forceinline__ void first_ticket(uint32_t* counter, uint32_t T, uint32_t min_chunks, uint32_t& tq,
+                                             uint32_t& mq)
+{
+    mq = max(ticket_chunks(T), min_chunks);
+    tq = atomicAdd(counter, mq);
+}
+// Compression's next chunk (T: none left).  [nx, nx_end) are the chunks of
+// the ticket in hand not started yet; (tq, mq) is the ticket drawn ahead.
+// Taking a ticket in hand draws the next one at once, so the atomic's round
+// trip overlaps the work on the ticket's chunks; a CTA draws no more once a
+// draw comes back at or past T.
+__device__ __forceinline__ uint32_t take_chunk(uint32_t* counter, uint32_t T, uint32_t& nx, uint32_t& nx_end,
+                                               uint32_t& tq, uint32_t& mq)
+{
+    if (nx < nx_end) return nx++;
+    const uint32_t t = tq;
+    if (t >= T) return T;
+    const uint32_t end = t + mq;
+    nx = t + 1;
+    nx_end = end < T ? end : T;
+    mq = ticket_chunks(end < T ? T - end : 0u);
+    tq = atomicAdd(counter, mq);
     return t;
 }
 

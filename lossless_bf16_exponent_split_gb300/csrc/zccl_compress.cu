@@ -15,8 +15,9 @@
 // contiguous run per CTA for the scan.  No CTA ever waits for the whole grid.
 //
 //  Phase 1 streams the input once.  CTAs take chunks by atomic ticket (SMs
-//    that get their data faster take more chunks; each ticket is drawn one
-//    chunk before it is needed).  Each chunk's 8 KB arrives
+//    that get their data faster take more chunks; a ticket is 4, 2 or 1
+//    consecutive chunks, smaller as the call nears its end, and each is drawn
+//    while the one before is being coded).  Each chunk's 8 KB arrives
 //    in shared memory by a TMA bulk copy, double-buffered so the next chunk
 //    lands while this one is coded.  A thread codes 8 consecutive elements
 //    from one 16-byte shared load: byte permutes give the sign-mantissa
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     uint32_t coded = 0;    // bookkeeper: chunks this CTA coded
     bool last = false;     // bookkeeper: this CTA completed the call's done count
     if (tid == 0) calls = call_read(a.ctrl);
-    uint32_t tn_pf = 0xFFFFFFFFu;  // thread 0: the ticket after next, drawn one chunk ahead
+    uint32_t nx = 0, nx_end = 0, tq = 0, mq = 0;  // thread 0: tickets (take_chunk)
     for (int e = tid; e < 256; e += kThreads) {
         uint32_t c = 0;
 #pragma unroll
@@ -325,24 +326,19 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
         mbar_init(&sm.bar[1], 1);
         fence_mbar_init();
         sm.abort = 0;
-        const uint32_t t = consume_ticket(a.ctrl, draw_ticket(a.ctrl), T);
+        first_ticket(&a.ctrl->ticket, T, 1u, tq, mq);
+        const uint32_t t = take_chunk(&a.ctrl->ticket, T, nx, nx_end, tq, mq);
         sm.next[0] = t;
-        if (t < T) {
-            sm.nseg[0] = issue_chunk_load(a, ustart, sm, t, 0);
-            tn_pf = draw_ticket(a.ctrl);
-        }
+        if (t < T) sm.nseg[0] = issue_chunk_load(a, ustart, sm, t, 0);
     }
     __syncthreads();
     uint32_t c = sm.next[0], k = 0;
     while (c < T) {
         const int buf = k & 1;
         if (tid == 0) {  // the next chunk (the load of this one is in flight)
-            const uint32_t tn = consume_ticket(a.ctrl, tn_pf, T);
+            const uint32_t tn = take_chunk(&a.ctrl->ticket, T, nx, nx_end, tq, mq);
             sm.next[(k + 1) & 1] = tn;
-            if (tn < T) {
-                sm.nseg[(k + 1) & 1] = issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
-                tn_pf = draw_ticket(a.ctrl);
-            }
+            if (tn < T) sm.nseg[(k + 1) & 1] = issue_chunk_load(a, ustart, sm, tn, buf ^ 1);
             if (k == 0) sm.calls = calls;  // for the bookkeeper, after the first chunk
         }
         const uint32_t s = sm.nseg[k & 1];  // (found by thread 0 when it started the load)
@@ -396,7 +392,10 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     }
     __syncthreads();
     const uint32_t par = sm.par;
-    if (tid == kBookkeeper) last = atom_add_release_u32(&a.ctrl->done[par], coded + 1) + coded + 1 == T + G;
+    if (tid == kBookkeeper) {
+        last = atom_add_release_u32(&a.ctrl->done[par], coded + 1) + coded + 1 == T + G;
+        if (last) st_relaxed_u32(&a.ctrl->ticket, 0u);  // every draw of the call has returned
+    }
     clear_other_parity(a.ctrl, a.flags, par);
     const uint64_t* acc = a.flags + (uint64_t)par * kFlagWords;
 

@@ -238,8 +238,10 @@ def test_workspace_scratch_left_zero(codec):
 
 def test_long_runs_full_parity(codec):
     """700M elements: each CTA's run of chunks spans more than one 128-chunk
-    batch in both kernels (grid <= 1216 CTAs), with a ragged tail; stream and
-    round trip bit-exact against the oracle."""
+    batch in both kernels (grid <= 1216 CTAs), with a ragged tail, and both
+    kernels hand out chunks in tickets of 4, then 2, then 1 consecutive
+    chunks as the call nears its end; stream and round trip bit-exact
+    against the oracle."""
     n = 700_000_000
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
