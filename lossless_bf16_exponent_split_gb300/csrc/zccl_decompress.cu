@@ -478,6 +478,9 @@ __device__ __forceinline__ uint32_t next_or_draw(uint32_t* counter, uint32_t& nx
     return kDrawn;
 }
 
+// kMulti: tickets of several chunks (calls of at least 16 x grid chunks); the
+// other instantiation keeps one-chunk tickets with no ticket-in-hand state.
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const DecompressArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -578,13 +581,13 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             published = atomicAdd(&a.ctrl->done[par], 1u);
             // the first two chunks (by ticket): their blocks need no offsets,
             // so start them now; the arrival comes with their zero-point copy
-            const uint32_t m0 = max(stream_ticket_chunks(T), 2u);
+            const uint32_t m0 = kMulti ? max(stream_ticket_chunks(T), 2u) : 2u;
             const uint32_t t = atomicAdd(&a.ctrl->dticket[par], m0);
             for (int i = 0; i < 2; ++i) {
                 sm.chunk[i] = t + i;
                 if (t + i < T) start_block(a, sm, t + i, i);
             }
-            hand_ticket(t, m0, 2u, T, nx, nx_end, mq);
+            if constexpr (kMulti) hand_ticket(t, m0, 2u, T, nx, nx_end, mq);
         } else {
             if (sm.abort) report(a.status, ZCCL_ERR_TIMEOUT);
             else if (b == 0) report(a.status, ZCCL_ERR_CORRUPT_STREAM);
@@ -663,7 +666,9 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
         } else {
             for (int i = 0; i < 2; ++i)
                 if (sm.chunk[i] < T) start_zp(a, sm, i, sm.chunk[i], e[i]);
-            if (sm.chunk[1] < T) tn = next_or_draw(&a.ctrl->dticket[par], nx, nx_end, tq, mq);
+            if (sm.chunk[1] < T)
+                tn = kMulti ? next_or_draw(&a.ctrl->dticket[par], nx, nx_end, tq, mq)
+                            : atomicAdd(&a.ctrl->dticket[par], 1u);
         }
     }
     __syncthreads();
@@ -687,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             break;
         }
         if (tid == 0) {
-            if (tn == kDrawn) {  // the draw made at the last refill
+            if (kMulti && tn == kDrawn) {  // the draw made at the last refill
                 const uint32_t t = tq;
                 tn = t < T ? t : T;
                 if (t < T) hand_ticket(t, mq, 1u, T, nx, nx_end, mq);
@@ -713,7 +718,8 @@ __global__ void __launch_bounds__(kThreads, 8) decompress_kernel(const Decompres
             if (t < T) {
                 start_block(a, sm, t, buf);
                 start_zp(a, sm, buf, t, en);
-                tn = next_or_draw(&a.ctrl->dticket[par], nx, nx_end, tq, mq);
+                tn = kMulti ? next_or_draw(&a.ctrl->dticket[par], nx, nx_end, tq, mq)
+                            : atomicAdd(&a.ctrl->dticket[par], 1u);
             } else {
                 tn = T;
             }
@@ -744,12 +750,19 @@ cudaError_t launch_scan(const ScanArgs& a, uint32_t grid, cudaStream_t stream)
 cudaError_t launch_decompress(const DecompressArgs& a, uint32_t grid, cudaStream_t stream)
 {
     const size_t smem = sizeof(DecodeSmem);
-    cudaError_t e = cudaFuncSetAttribute(decompress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const bool multi = units_of(a.n) >= 16ull * grid;  // (the kernel's first ticket is then 2 or 4 chunks)
+    auto kernel = multi ? decompress_kernel<true> : decompress_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_cooperative(decompress_kernel, grid, kThreads, smem, stream, a);
+    return launch_cooperative(kernel, grid, kThreads, smem, stream, a);
 }
 
 int scan_ctas_per_sm() { return occupancy(escape_scan_kernel, 0); }
-int decompress_ctas_per_sm() { return occupancy(decompress_kernel, sizeof(DecodeSmem)); }
+int decompress_ctas_per_sm()
+{
+    const int one = occupancy(decompress_kernel<false>, sizeof(DecodeSmem));
+    const int multi = occupancy(decompress_kernel<true>, sizeof(DecodeSmem));
+    return one < multi ? one : multi;
+}
 
 }  // namespace zccl
