@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     // final once its count says the run is complete, and a chunk count once
     // it is nonzero, so both are loaded before the wait; only what was not
     // final yet is loaded again after it.  (The staged escape bytes are read
-    // only after the wait and its acquire fence.)
+    // only after the wait and its acquire load.)
     const uint32_t st = ustart[find_segment(ustart, a.n_segs, lo)];
     const uint32_t h0 = st < lo ? run_of(st, sh) : b;  // flag words [h0, b) make the carry
     uint64_t part = 0;
@@ -458,7 +458,11 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const CompressArgs a
     uint32_t cnt0 = tid < (int)nb0 ? __ldcg(a.counts + lo + tid) : 1u;  // my chunk count + 1 (first batch)
     if (tid == 0) {
         const bool ok = wait_count(&a.ctrl->done[par], T + G);
-        fence_acq_rel_gpu();  // what the coders wrote before counting themselves done
+        // acquire the count that the poll saw complete: it was made by a chain
+        // of release adds, one per CTA, so every coder's writes are ordered
+        // before what follows (cheaper than a full fence, which also waits for
+        // this thread's own stores)
+        (void)ld_acquire_u32(&a.ctrl->done[par]);
         if (!ok) sm.abort = 1;
     }
     __syncthreads();
