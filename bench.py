@@ -15,7 +15,8 @@ timed means.  Other workloads (--workload): activation_mix (compress +
 decompress), moe_a2a (one batched compress of 128 static/dynamic segments),
 rs_local (decompress-reduce of 8 shards), rs_local_own (the same with the rank's own shard
 uncompressed), activation_mix_lut (the exponent histogram pass that measures
-a LUT from the data), gauss1m.
+a LUT from the data), gauss1m, gauss268m (one stream of 268M elements, the
+same distribution as the default).
 
 Prints ONE JSON line (rank 0).  `value` = GB/s of BF16 input through the step
 (2n bytes per compress and per decompress; reduce: 2 S n; histogram: 2n),
@@ -51,7 +52,7 @@ def parse_args():
     p.add_argument("--impl", default="zccl", choices=["zccl", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=["llama3_8b_allgather", "activation_mix", "moe_a2a", "rs_local", "rs_local_own",
-                            "activation_mix_lut", "gauss1m"])
+                            "activation_mix_lut", "gauss1m", "gauss268m"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-configs", action="store_true",
@@ -354,7 +355,7 @@ def make_inputs(name, seed):
     """Host arrays for a workload: (kind, payload(s), sigma, extra)."""
     from lossless_bf16_exponent_split_gb300 import workloads as w
     cfg = w.CONFIGS[name]
-    if name in ("llama3_8b_allgather", "gauss1m"):
+    if name in ("llama3_8b_allgather", "gauss1m", "gauss268m"):
         return "roundtrip", w.gaussian(cfg["n"], cfg["sigma"], seed=seed), cfg["sigma"], None
     if name == "activation_mix":
         return "roundtrip", w.activation_mix(seed=seed), cfg["sigma"], None
@@ -590,7 +591,8 @@ def main():
             cfg_extra = {"n": n, "stream_bytes": stream_bytes, "ratio": round(stream_bytes / (2 * n), 5),
                          "step": "compress batch k + decompress the stream of batch k-1 (k+1 in the rotation "
                                  "when k-1's buffer is the one the compress batch wrote last)",
-                         "l2": "3 rotating buffer sets, >316 MB touched per step (> 129 MB L2)"}
+                         "l2": f"3 rotating buffer sets, {(4 * n + stream_bytes) / 1e6:.0f} MB touched per step "
+                               "(> 129 MB L2)"}
         elif kind == "batched":
             m = extra
             payload = tdev(host)

@@ -126,6 +126,8 @@ def special_values(n: int, seed: int = 0, frac: float = 0.3) -> np.ndarray:
 # Workload table: sizes and value recipes of the five standard configurations.
 CONFIGS = {
     "gauss1m": dict(n=1_048_576, sigma=0.02, desc="1,048,576 BF16 N(0, 0.02^2), seed 0"),
+    "gauss268m": dict(n=1 << 28, sigma=0.02,
+                      desc="268,435,456 BF16 N(0, 0.02^2), seed 0: one large stream (a 512 MB all-gather bucket)"),
     "llama3_8b_allgather": dict(n=4096 * 14336, sigma=0.02,
                                 desc="4096x14336 BF16 N(0, 0.02^2), seed 0"),
     "activation_mix": dict(n=8192 * 4096, sigma=1.0,
