@@ -476,7 +476,8 @@ __device__ __forceinline__ void call_end(WsCtrl* ctrl, uint32_t calls, bool last
     if (last) st_relaxed_u32(&ctrl->calls, calls + 1);
 }
 
-// Thread 0: chunk tickets from one counter.  A ticket is a run of
+// Thread 0 of compression: chunk tickets from one counter (decompression
+// sizes its own, in its kernel).  A ticket is a run of
 // consecutive chunks: 4 while at least 16 x gridDim.x chunks remain after it,
 // 2 while at least 4 x gridDim.x do, then 1, so the counter sees a quarter of
 // the draws for most of a large call and the tail still balances chunk by
