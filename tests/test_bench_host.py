@@ -32,3 +32,23 @@ def test_group_bounds_cover_every_launch_once():
         sizes = [b[i + 1] - b[i] for i in range(len(b) - 1)]
         assert all(x >= 1 for x in sizes)
         assert max(sizes) - min(sizes) <= 1
+
+
+def test_every_workload_is_a_bench_choice_with_a_kind(monkeypatch):
+    """Each entry of the workload table is accepted by --workload and maps to
+    one of the measurement kinds (the generators are stubbed, so no payload
+    is built)."""
+    import sys
+    from lossless_bf16_exponent_split_gb300 import workloads as w
+    tiny = w.gaussian(16, 0.02, seed=0)
+    monkeypatch.setattr(w, "gaussian", lambda n, sigma, seed=0: tiny)
+    monkeypatch.setattr(w, "activation_mix", lambda *a, **k: tiny)
+    monkeypatch.setattr(w, "moe_payload", lambda **k: type("M", (), {"payload": tiny})())
+    monkeypatch.setattr(w, "reduce_shards", lambda S, n, sigma, seed=0: [tiny] * S)
+    for name in w.CONFIGS:
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", name])
+        assert bench.parse_args().workload == name
+        assert bench.make_inputs(name, 0)[0] in ("roundtrip", "histogram", "batched", "reduce")
+    assert bench.make_inputs("gauss268m", 0)[0] == "roundtrip"
+    assert w.CONFIGS["gauss268m"]["n"] == 1 << 28
+    assert "gauss268m" not in bench.CONFIG_WORKLOADS  # opt-in: not part of the default run
